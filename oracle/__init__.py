@@ -1,0 +1,42 @@
+"""Float64 CPU oracle for exact tiled attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import, call or execute anything
+in this package.  The product path (the CUDA library under
+``exact_tiled_attention_11_gb300`` and its Python binding) never imports it,
+and this package imports nothing from the product: the two share no code.
+Only the seeded input generators (``exact_tiled_attention_11_gb300.workloads``,
+which hold none of the attention arithmetic) feed both sides.
+
+Everything is plain NumPy in float64, one (batch, head) at a time, written so
+that it can be checked against the pages by eye:
+
+* ``attention``        -- the plain definition (materialised S, stable softmax,
+                          P.V, log-sum-exp), which exact tiled attention reaches
+                          up to rounding order.
+* ``tiled_attention``  -- the block-wise algorithm itself (online softmax over
+                          K/V tiles, causal tile skipping), reporting the block
+                          pairs it visited.
+* ``partial_state`` / ``merge_partials`` / ``finalize`` -- the (m, l, o~)
+                          partial results over a key subset and their exact
+                          merge rule.
+* ``decode_paged``     -- one query token per sequence against a paged, ragged
+                          KV cache gathered through a page table.
+
+Pins (``tests/test_oracle_pins.py``, ``-m "not gpu"``): the worked examples the
+pages print, a scalar pure-Python brute force on tiny inputs, closed forms
+(K = 0, one key), invariants (block-shape independence, partition/merge
+independence, convex combination, no overflow at large scores) and the causal
+block-pair counts the pages report.  No function here is unpinned.
+"""
+from .attention import (  # noqa: F401
+    attention,
+    attention_rows,
+    tiled_attention,
+    partial_state,
+    merge_partials,
+    finalize,
+    decode_paged,
+    gather_sequence,
+    to_f64,
+)
