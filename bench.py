@@ -1,0 +1,453 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact tiled attention hot path on GB300.
+
+One step is one pass over both halves of the hot path, each on its
+full-size synthetic workload, with inputs resident in HBM:
+  prefill  attn_fwd, bf16, causal, B=1, H=32, Hkv=8, N=8192, d=128
+  decode   attn_decode_paged, bf16, 64 sequences x 1 token, H=32, Hkv=8, d=128,
+           KV lengths uniform in [512, 32768], page size 16, pages at a random
+           permutation of the pool (split kernel + merge kernel)
+``value`` is the prefill throughput in TFLOP/s (4 N^2 d B H / 2 for causal),
+the decode throughput is reported in GB/s beside it, each with its roofline.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+With --gpus N > 1 it runs under torch.distributed.run, one independent replica
+per GPU (the path has no exchange step), and reports the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefill attention TFLOP/s & split-KV decode HBM GB/s on 1 GB300 (% roofline)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ peaks and clocks
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = []
+        for line in self.out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        loaded = [r for r in rows if r[2] > 200.0] or rows   # samples drawing real power
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ ncu traffic records
+
+def kernel_source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "exact_tiled_attention_11_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "prefill_bf16": ["prefill_bf16.cu", "tc05.cuh", "common.cuh"],
+    "decode_split": ["decode.cu", "common.cuh"],
+}
+
+
+def recorded_traffic(name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(name)
+    if not rec or rec.get("source_sha") != kernel_source_sha(KERNEL_SOURCES[name]):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ workload
+
+def make_inputs(dev, seed=0):
+    import torch
+    from exact_tiled_attention_11_gb300 import workloads as W
+    q, k, v = W.prefill_inputs_for(W.C3, seed=seed)
+    kv = W.decode_inputs_for(W.C4, seed=seed)
+    host = {"q": q, "k": k, "v": v, "dq": kv.q, "page_table": kv.page_table, "kv_lens": kv.kv_lens}
+    d = {
+        "q": q.to(dev), "k": k.to(dev), "v": v.to(dev),
+        "dq": kv.q.to(dev), "k_pages": kv.k_pages.to(dev), "v_pages": kv.v_pages.to(dev),
+        "page_table": kv.page_table.to(dev), "kv_lens": kv.kv_lens.to(dev),
+    }
+    d["o"] = torch.empty_like(d["q"])
+    d["lse"] = torch.empty(W.C3.B, W.C3.H, W.C3.N, dtype=torch.float32, device=dev)
+    d["do"] = torch.empty(W.C4.B, W.C4.H, W.C4.d, dtype=torch.bfloat16, device=dev)
+    d["dlse"] = torch.empty(W.C4.B, W.C4.H, dtype=torch.float32, device=dev)
+    return host, d, kv
+
+
+def decode_bytes(kv):
+    """Algorithmic bytes of one decode: K/V of the attended tokens, q, page table
+    entries used, kv_lens, O (bf16) and LSE written."""
+    import torch
+    B, H, d = kv.q.shape
+    pages_used = int(((kv.kv_lens.to(torch.int64) + kv.page_size - 1) // kv.page_size).sum())
+    return kv.kv_bytes() + kv.q.numel() * 2 + pages_used * 4 + B * 4 + B * H * d * 2 + B * H * 4
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+
+def oracle_prefill_sample(q, k, v, heads, rows, scale):
+    """Time the float64 oracle on sampled (head, rows) of the long causal workload; return (flops, seconds)."""
+    import numpy as np
+    import oracle
+    t0 = time.perf_counter()
+    flops = 0.0
+    d = q.shape[-1]
+    for h in heads:
+        oracle.attention_rows(q, k, v, 0, h, rows, causal=True, scale=scale)
+        flops += float(np.sum(4.0 * (rows + 1) * d))    # causal: row r attends r + 1 keys
+    return flops, time.perf_counter() - t0
+
+
+def oracle_decode_sample(kv, seqs, scale):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.decode_paged(kv.q, kv.k_pages, kv.v_pages, kv.page_table, kv.kv_lens, scale=scale, seqs=seqs)
+    dt = time.perf_counter() - t0
+    Hkv, d = kv.k_pages.shape[1], kv.k_pages.shape[3]
+    nbytes = sum(int(kv.kv_lens[b]) for b in seqs) * Hkv * d * 2 * 2
+    return nbytes, dt
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+PREFILL_SAMPLE = {"heads": [0, 9, 18, 27], "rows": 2048}
+DECODE_SAMPLE_SEQS = [0, 7, 21, 42]
+
+
+def cpu_baseline(host, kv):
+    import numpy as np
+    from exact_tiled_attention_11_gb300 import workloads as W
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(W.C3.N, PREFILL_SAMPLE["rows"], replace=False))
+    fl, dt = oracle_prefill_sample(host["q"], host["k"], host["v"], PREFILL_SAMPLE["heads"], rows, W.C3.scale)
+    nb, ddt = oracle_decode_sample(kv, DECODE_SAMPLE_SEQS, W.C4.scale)
+    return {
+        "value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+        "sample": (f"float64 NumPy oracle, prefill: {len(PREFILL_SAMPLE['heads'])} heads x {len(rows)} random query "
+                   f"rows of the N=8192 causal workload ({fl:.3g} algorithmic FLOP in {dt:.2f} s); decode: "
+                   f"{len(DECODE_SAMPLE_SEQS)} of 64 sequences ({nb / 1e9:.3f} GB of K/V in {ddt:.2f} s)"),
+        "decode": {"value": nb / ddt / 1e9, "unit": "GB/s"},
+    }
+
+
+# ------------------------------------------------------------------ the reference arm: the oracle on the host
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import numpy as np
+    from exact_tiled_attention_11_gb300 import workloads as W
+    q, k, v = W.prefill_inputs_for(W.C3)
+    rng = np.random.default_rng(0)
+    per_step_rows = 256
+    times, flops = [], []
+    for i in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(W.C3.N, per_step_rows, replace=False))
+        fl, dt = oracle_prefill_sample(q, k, v, [i % W.C3.H], rows, W.C3.scale)
+        if i >= args.warmup:
+            times.append(dt)
+            flops.append(fl)
+    value = sum(flops) / sum(times) / 1e12
+    ms = 1e3 * sum(times) / len(times)
+    sample = (f"each step: float64 NumPy oracle on {per_step_rows} random query rows of one head of the "
+              f"N=8192 causal workload (one (b, h) slice; heads cycle per step)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": W.C3.name, "parallelism": "host cores (oracle)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+    import exact_tiled_attention_11_gb300 as lib
+    from exact_tiled_attention_11_gb300 import workloads as W
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib.load_library()
+    stream = torch.cuda.current_stream(dev)
+
+    host, d, kv = make_inputs(dev)
+    pre_flops = W.C3.flops(causal=True)
+    dec_bytes = decode_bytes(kv)
+    splits = lib.attn_decode_max_splits(W.C4.B, W.C4.H, W.C4.Hkv, kv.max_pages)
+    ws = torch.empty(lib.attn_decode_workspace_size(W.C4.B, W.C4.H, W.C4.d, splits), dtype=torch.uint8, device=dev)
+
+    def prefill():
+        lib.attn_fwd(d["q"], d["k"], d["v"], d["o"], d["lse"], causal=True, scale=W.C3.scale)
+
+    def decode():
+        lib.attn_decode_paged(d["dq"], d["k_pages"], d["v_pages"], d["page_table"], d["kv_lens"], d["do"],
+                              d["dlse"], scale=W.C4.scale, num_splits=0, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        prefill()
+        decode()
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local_rank) as clk:
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            prefill()
+            ev[i][1].record(stream)
+            decode()
+            ev[i][2].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = start.elapsed_time(stop)
+    pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    if lib.attn_device_error() != 0:
+        raise SystemExit("a kernel recorded a device error during the benchmark")
+
+    elapsed_ms = reduce_max(elapsed_ms, world)
+    pre_tot = reduce_max(sum(pre_ms), world)
+    dec_tot = reduce_max(sum(dec_ms), world)
+    ms_per_step = elapsed_ms / args.steps
+    pre_tflops = world * pre_flops * args.steps / (pre_tot * 1e-3) / 1e12
+    dec_gbs = world * dec_bytes * args.steps / (dec_tot * 1e-3) / 1e9
+
+    # ---------------- end to end through the public API: pinned host buffers, copies inside the timed region
+    e2e = None
+    if rank == 0 or world > 1:
+        pin = {n: host[n].pin_memory() for n in ("q", "k", "v", "dq", "page_table", "kv_lens")}
+        out_o = torch.empty(d["o"].shape, dtype=d["o"].dtype).pin_memory()
+        out_lse = torch.empty(d["lse"].shape, dtype=torch.float32).pin_memory()
+        out_do = torch.empty(d["do"].shape, dtype=d["do"].dtype).pin_memory()
+        out_dlse = torch.empty(d["dlse"].shape, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = sum(t.numel() * t.element_size() for t in (out_o, out_lse, out_do, out_dlse))
+        pre_h2d = sum(pin[n].numel() * pin[n].element_size() for n in ("q", "k", "v"))
+
+        def e2e_step(evs):
+            evs[0].record(stream)
+            for n, dst in (("q", "q"), ("k", "k"), ("v", "v")):
+                d[dst].copy_(pin[n], non_blocking=True)
+            prefill()
+            out_o.copy_(d["o"], non_blocking=True)
+            out_lse.copy_(d["lse"], non_blocking=True)
+            evs[1].record(stream)
+            d["dq"].copy_(pin["dq"], non_blocking=True)
+            d["page_table"].copy_(pin["page_table"], non_blocking=True)
+            d["kv_lens"].copy_(pin["kv_lens"], non_blocking=True)
+            decode()
+            out_do.copy_(d["do"], non_blocking=True)
+            out_dlse.copy_(d["dlse"], non_blocking=True)
+            evs[2].record(stream)
+
+        for _ in range(max(args.warmup, 3)):
+            e2e_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+        torch.cuda.synchronize()
+        eev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        barrier(world)
+        for i in range(args.steps):
+            e2e_step(eev[i])
+        torch.cuda.synchronize()
+        barrier(world)
+        e_pre = reduce_max(sum(e[0].elapsed_time(e[1]) for e in eev), world)
+        e_dec = reduce_max(sum(e[1].elapsed_time(e[2]) for e in eev), world)
+        e2e = {"value": world * pre_flops * args.steps / (e_pre * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "prefill_h2d_bytes_per_step": pre_h2d,
+               "decode": {"value": world * dec_bytes * args.steps / (e_dec * 1e-3) / 1e9, "unit": "GB/s"},
+               "ms_per_step": (e_pre + e_dec) / args.steps,
+               "note": "decode KV pool is device-resident cache state; per step only q, page table and kv_lens go H2D"}
+
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = load_peaks()
+    t_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    pre_avg_s = pre_tot / args.steps * 1e-3 / 1.0
+    dec_avg_s = dec_tot / args.steps * 1e-3
+    pre_launch_tflops = pre_flops / pre_avg_s / 1e12
+    dec_launch_gbs = dec_bytes / dec_avg_s / 1e9
+    roof_pre = {"bound": "tensor", "achieved": pre_launch_tflops, "peak": t_peak, "unit": "TFLOP/s",
+                "frac": pre_launch_tflops / t_peak, "traffic": recorded_traffic("prefill_bf16"),
+                "kernel": "prefill_bf16_kernel<128>", "peak_source": f"{peak_src} bf16_tflops (burst)",
+                "algorithmic_flops_per_launch": pre_flops}
+    roof_dec = {"bound": "hbm", "achieved": dec_launch_gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": dec_launch_gbs / hbm_peak, "traffic": recorded_traffic("decode_split"),
+                "kernel": "decode_split_kernel + merge_kernel (one attn_decode_paged call)",
+                "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": dec_bytes}
+    dominant = roof_dec if dec_tot > pre_tot else roof_pre
+    clocks = clk.summary()
+
+    line = {
+        "metric": METRIC, "value": pre_tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": f"{W.C3.name} + {W.C4.name}",
+            "prefill": "attn_fwd bf16 causal B=1 H=32 Hkv=8 N=8192 d=128 scale=1/sqrt(128)",
+            "decode": (f"attn_decode_paged bf16 B=64 H=32 Hkv=8 d=128 page=16 lengths randint[512,32768] seed 0 "
+                       f"(pool {kv.k_pages.shape[0]} pages), auto split count {splits}"),
+            "l2": "no flush; every input set is larger than L2 (prefill 160 MiB touched, decode streams 4.1 GB per step)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "decode": {"value": dec_gbs, "unit": "GB/s", "frac_of_hbm": dec_gbs / hbm_peak,
+                   "ms_per_call": dec_tot / args.steps},
+        "prefill": {"value": pre_tflops, "unit": "TFLOP/s", "frac_of_bf16": pre_tflops / t_peak,
+                    "ms_per_call": pre_tot / args.steps},
+        "roofline": dominant,
+        "rooflines": {"prefill": roof_pre, "decode": roof_dec},
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(host, kv)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" and torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, rank, world)
+        return run_ours(args, rank, local_rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

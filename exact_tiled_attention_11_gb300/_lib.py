@@ -1,0 +1,188 @@
+"""ctypes binding over libattn.so: the C ABI of include/attn.h, same names.
+
+Only argument marshalling happens here: shapes and dtypes are read from
+torch tensors, outputs the caller did not supply are allocated with torch,
+and the raw device pointers plus the current CUDA stream are handed to the
+library.  Every step of the computation runs in the library's kernels.  If
+the library has not been built, every call raises instead of falling back to
+anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from ._build import LIB_PATH
+
+ATTN_F32 = 0
+ATTN_BF16 = 1
+_STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_WORKSPACE",
+           4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_DEVICE_CHECK"}
+
+_lock = threading.Lock()
+_handle = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {_STATUS.get(status, status)}")
+        self.status = status
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libattn.so (built by ``exact_tiled_attention_11_gb300._build.build``)."""
+    global _handle
+    with _lock:
+        if _handle is not None:
+            return _handle
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+                              "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.attn_fwd.restype = i32
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp]
+        lib.attn_decode_workspace_size.restype = sz
+        lib.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+        lib.attn_decode_max_splits.restype = i32
+        lib.attn_decode_max_splits.argtypes = [i32, i32, i32, i32]
+        lib.attn_decode_paged.restype = i32
+        lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32,
+                                          vp, sz, vp]
+        lib.merge_partials.restype = i32
+        lib.merge_partials.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, i32, vp, vp]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_status_string.argtypes = [i32]
+        lib.attn_device_error.restype = i32
+        lib.attn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+        _handle = lib
+        return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise AttnError(fn, status)
+
+
+def _need(t, name, dtype=None, ndim=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(status).decode()
+
+
+def attn_fwd(q, k, v, o=None, lse=None, *, causal=False, scale=None, stream=None):
+    """Exact attention forward pass.  q [B, H, N, d]; k, v [B, Hkv, N, d]; bf16 or fp32.
+
+    Returns (o [B, H, N, d] in q's dtype, lse [B, H, N] fp32)."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, 4)
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("attn_fwd takes bf16 or fp32 tensors")
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, N, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, N, d] matching q")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, N, dtype=torch.float32, device=q.device)
+    _need(o, "o", q.dtype, 4)
+    _need(lse, "lse", torch.float32, 3)
+    scale = (1.0 / d ** 0.5) if scale is None else float(scale)
+    dt = ATTN_BF16 if q.dtype == torch.bfloat16 else ATTN_F32
+    _check("attn_fwd", lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d,
+                                    1 if causal else 0, scale, dt, _stream(stream, q.device)))
+    return o, lse
+
+
+def attn_decode_workspace_size(B: int, H: int, d: int, max_splits: int) -> int:
+    return int(load_library().attn_decode_workspace_size(B, H, d, max_splits))
+
+
+def attn_decode_max_splits(B: int, H: int, Hkv: int, max_pages_per_seq: int) -> int:
+    return int(load_library().attn_decode_max_splits(B, H, Hkv, max_pages_per_seq))
+
+
+def attn_decode_paged(q, k_pages, v_pages, page_table, kv_lens, o=None, lse=None, *, scale=None, num_splits=0,
+                      workspace=None, stream=None):
+    """Split-KV decode over a paged cache.  q [B, H, d] bf16; k_pages, v_pages
+    [P, Hkv, page_size, d] bf16; page_table [B, max_pages] int32; kv_lens [B] int32.
+
+    Returns (o [B, H, d] bf16, lse [B, H] fp32).  ``workspace`` (uint8, device)
+    is allocated here when not given."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(kv_lens, "kv_lens", torch.int32, 1)
+    B, H, d = q.shape
+    P, Hkv, ps, _ = k_pages.shape
+    maxp = page_table.shape[1]
+    if o is None:
+        o = torch.empty(B, H, d, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, H, dtype=torch.float32, device=q.device)
+    S = num_splits if num_splits > 0 else lib.attn_decode_max_splits(B, H, Hkv, max(maxp, 1))
+    need = lib.attn_decode_workspace_size(B, H, d, max(S, 1))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check("attn_decode_paged", lib.attn_decode_paged(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens), _ptr(o), _ptr(lse),
+        B, H, Hkv, d, ps, maxp, P, (1.0 / d ** 0.5) if scale is None else float(scale), int(num_splits),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream, q.device)))
+    return o, lse
+
+
+def merge_partials(m, l, o_tilde, num_parts=None, *, out_dtype=torch.bfloat16, o=None, lse=None, stream=None):
+    """Exact merge of partials: m, l [B, H, S] fp32, o_tilde [B, H, S, d] fp32,
+    num_parts [B] int32 or None.  Returns (o [B, H, d] out_dtype, lse [B, H] fp32)."""
+    lib = load_library()
+    _need(m, "m", torch.float32, 3)
+    _need(l, "l", torch.float32, 3)
+    _need(o_tilde, "o_tilde", torch.float32, 4)
+    B, H, S, d = o_tilde.shape
+    if num_parts is not None:
+        _need(num_parts, "num_parts", torch.int32, 1)
+    if o is None:
+        o = torch.empty(B, H, d, dtype=out_dtype, device=m.device)
+    if lse is None:
+        lse = torch.empty(B, H, dtype=torch.float32, device=m.device)
+    dt = ATTN_BF16 if o.dtype == torch.bfloat16 else ATTN_F32
+    _check("merge_partials", lib.merge_partials(_ptr(m), _ptr(l), _ptr(o_tilde), _ptr(num_parts), B, H, S, d,
+                                                _ptr(o), dt, _ptr(lse), _stream(stream, m.device)))
+    return o, lse
+
+
+def attn_device_error(clear: bool = False) -> int:
+    """The OR of the kernels' device error words (synchronises the device)."""
+    code = ctypes.c_uint32(0)
+    _check("attn_device_error", load_library().attn_device_error(ctypes.byref(code), 1 if clear else 0))
+    return int(code.value)

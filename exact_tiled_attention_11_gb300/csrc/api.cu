@@ -1,0 +1,195 @@
+// Host side of the C ABI declared in include/attn.h: argument validation,
+// TMA tensor-map encoding, the split-KV plan, and kernel launches.  Nothing
+// here allocates device memory or synchronises (except attn_device_error).
+#include <algorithm>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "attn.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+using attn::PrefillMaps;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 tensor [d2][d1][d0] (d0 contiguous) with a box of (64, box1, 1) and 128-byte swizzle.
+bool make_map_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box1) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {64, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Split-KV plan from arguments only (no device-to-host copy): enough
+// (sequence, KV head, chunk) CTAs for ~6 per SM when every sequence is as long
+// as the longest, chunks of at most 64 and at least 8 pages.
+int auto_splits(int B, int Hkv, int max_pages, int num_sms) {
+  const int want_ctas = 6 * std::max(num_sms, 1);
+  int s = ceil_div(max_pages, 64);
+  s = std::max(s, ceil_div(want_ctas, static_cast<long long>(B) * Hkv));
+  s = std::min(s, ceil_div(max_pages, 8));
+  return std::max(s, 1);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" {
+
+const char *attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_DEVICE_CHECK: return "ATTN_ERR_DEVICE_CHECK";
+  }
+  return "ATTN_STATUS_UNKNOWN";
+}
+
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Hkv, int N,
+                       int d, int causal, float scale, attn_dtype_t dtype, attn_stream_t stream) {
+  if (B < 0 || H < 0 || Hkv < 0 || N < 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (Hkv == 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
+    return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (dtype == ATTN_F32) {
+    e = attn::launch_prefill_f32(static_cast<const float *>(q), static_cast<const float *>(k),
+                                 static_cast<const float *>(v), static_cast<float *>(o), lse, B, H, Hkv, N, d,
+                                 causal != 0, scale, st);
+  } else {
+    PrefillMaps maps;
+    if (!make_map_3d(&maps.q, q, d, N, static_cast<uint64_t>(B) * H, 128) ||
+        !make_map_3d(&maps.k, k, d, N, static_cast<uint64_t>(B) * Hkv, 128) ||
+        !make_map_3d(&maps.v, v, d, N, static_cast<uint64_t>(B) * Hkv, 128))
+      return ATTN_ERR_CUDA;
+    e = attn::launch_prefill_bf16(maps, o, lse, B, H, Hkv, N, d, causal != 0, scale, 0, st);
+  }
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_decode_workspace_size(int B, int H, int d, int max_splits) {
+  if (B <= 0 || H <= 0 || d <= 0 || max_splits <= 0) return 0;
+  const size_t n = static_cast<size_t>(B) * H * max_splits;
+  return 2 * align256(n * sizeof(float)) + align256(n * d * sizeof(float));
+}
+
+int attn_decode_max_splits(int B, int H, int Hkv, int max_pages_per_seq) {
+  if (B <= 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || max_pages_per_seq <= 0) return 0;
+  return auto_splits(B, Hkv, max_pages_per_seq, device_sm_count());
+}
+
+attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,
+                                const int32_t *kv_lens, void *o, float *lse, int B, int H, int Hkv, int d,
+                                int page_size, int max_pages_per_seq, int num_pages, float scale, int num_splits,
+                                void *workspace, size_t workspace_bytes, attn_stream_t stream) {
+  if (B < 0 || H < 0 || Hkv < 0 || max_pages_per_seq < 0 || num_pages < 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || H == 0) return ATTN_OK;
+  if (Hkv == 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (q == nullptr || o == nullptr || kv_lens == nullptr || workspace == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || (lse && !aligned16(lse)) || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
+  if (d != 128 || page_size != 16 || H / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
+  if (max_pages_per_seq > 0 && num_pages > 0) {
+    if (k_pages == nullptr || v_pages == nullptr || page_table == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(k_pages) || !aligned16(v_pages)) return ATTN_ERR_INVALID_ARG;
+  }
+  const int mp = std::max(max_pages_per_seq, 1);
+  const int S = num_splits > 0 ? std::min(num_splits, mp) : auto_splits(B, Hkv, mp, device_sm_count());
+  const int chunk = ceil_div(mp, S);
+  const int S_used = ceil_div(mp, chunk);  // partial slots any sequence can need
+  if (workspace_bytes < attn_decode_workspace_size(B, H, d, S_used)) return ATTN_ERR_WORKSPACE;
+  if (S_used > 65535 || B > 65535) return ATTN_ERR_UNSUPPORTED;
+
+  const size_t n = static_cast<size_t>(B) * H * S_used;
+  float *ws_m = static_cast<float *>(workspace);
+  float *ws_l = reinterpret_cast<float *>(static_cast<char *>(workspace) + align256(n * sizeof(float)));
+  float *ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + 2 * align256(n * sizeof(float)));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  if (max_pages_per_seq > 0 && num_pages > 0) {
+    CUtensorMap tm_k, tm_v;
+    const uint64_t rows = static_cast<uint64_t>(num_pages) * Hkv;
+    if (!make_map_3d(&tm_k, k_pages, d, page_size, rows, page_size) ||
+        !make_map_3d(&tm_v, v_pages, d, page_size, rows, page_size))
+      return ATTN_ERR_CUDA;
+    cudaError_t e = attn::launch_decode_split(tm_k, tm_v, q, page_table, kv_lens, ws_m, ws_l, ws_o, B, H, Hkv,
+                                              max_pages_per_seq, num_pages, chunk, S_used, scale, st);
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  // with no pages at all every sequence is empty: the merge writes O = 0, LSE = -inf
+  cudaError_t e = attn::launch_merge(ws_m, ws_l, ws_o, nullptr, kv_lens, page_size,
+                                     (max_pages_per_seq > 0 && num_pages > 0) ? chunk : 1 << 30, B, H, S_used, d, o,
+                                     true, lse, st);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t merge_partials(const float *m, const float *l, const float *o_tilde, const int32_t *num_parts, int B,
+                             int H, int S, int d, void *o, attn_dtype_t o_dtype, float *lse, attn_stream_t stream) {
+  if (B < 0 || H < 0 || S < 1) return ATTN_ERR_INVALID_ARG;
+  if (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || H == 0) return ATTN_OK;
+  if (m == nullptr || l == nullptr || o_tilde == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(o_tilde) || !aligned16(o) || (lse && !aligned16(lse))) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  cudaError_t e = attn::launch_merge(m, l, o_tilde, num_parts, nullptr, 0, 1, B, H, S, d, o, o_dtype == ATTN_BF16,
+                                     lse, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_device_error(uint32_t *code, int clear) {
+  if (code == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned int a = 0, b = 0, c = 0;
+  if (attn::device_error_decode(&a, clear != 0) != cudaSuccess ||
+      attn::device_error_prefill_f32(&b, clear != 0) != cudaSuccess ||
+      attn::device_error_prefill_bf16(&c, clear != 0) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  *code = a | b | c;
+  return ATTN_OK;
+}
+
+}  // extern "C"

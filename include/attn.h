@@ -1,0 +1,172 @@
+/*
+ * attn.h -- C ABI of the exact tiled attention library for GB300 (sm_103a).
+ *
+ * Exact block-wise (Flash) attention: the prefill forward pass and split-KV
+ * paged decode with the exact merge of partial results.  Every entry point
+ * takes plain device pointers and sizes, launches on the caller's CUDA
+ * stream and returns without synchronising.  The library allocates no
+ * device memory: the caller owns every buffer (including the decode
+ * workspace) and keeps it alive until the launched work has finished.
+ *
+ * Common rules
+ *  - Device pointers must be 16-byte aligned and tensors dense, last
+ *    dimension contiguous, in the layouts stated per call.
+ *  - Argument errors are detected on the host and returned before anything
+ *    is launched (ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
+ *    ATTN_ERR_WORKSPACE).  A failed launch returns ATTN_ERR_CUDA.  Kernel
+ *    faults surface, as with any CUDA call, at the next synchronising call.
+ *  - Kernels never trap.  Their pipeline waits are bounded; a wait that runs
+ *    out sets a device-wide error word and the kernel returns early.
+ *    attn_device_error() reads (and optionally clears) that word.
+ *  - Grouped-query attention: query head h reads KV head h / (H / Hkv); H
+ *    must be a multiple of Hkv.
+ *  - The log-sum-exp (LSE) is the natural logarithm of the sum of exp of the
+ *    scaled scores of a row; a row that attends to no key has O = 0 and
+ *    LSE = -inf.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers; NULL is the legacy default stream. */
+typedef struct CUstream_st *attn_stream_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative size, H % Hkv != 0, ... */
+  ATTN_ERR_UNSUPPORTED = 2,  /* a valid request this build has no kernel for (d, dtype, page size) */
+  ATTN_ERR_WORKSPACE = 3,    /* decode workspace smaller than attn_decode_workspace_size() */
+  ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call or a launch failed */
+  ATTN_ERR_DEVICE_CHECK = 5  /* a kernel recorded a failed in-kernel check (see attn_device_error) */
+} attn_status_t;
+
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+/*
+ * attn_fwd -- exact attention forward pass (prefill).
+ *
+ * Follows "3.4 Attention Kernels" (llm-learning-path), sections "Online
+ * softmax" and "FlashAttention: tiling": Q is cut into row tiles, K and V are
+ * streamed tile by tile through on-chip memory, each score tile
+ * S_ij = scale * Q_i K_j^T is folded into a running row maximum m, running
+ * denominator l and unnormalised output o~ with the online-softmax rescale
+ * exp(m - m'), and O_i = o~ / l and LSE_i = m + ln l are written once.  With
+ * causal = 1, key tiles wholly after a query tile are skipped and the
+ * diagonal tile is masked (key j is attended by query i iff j <= i).  Also
+ * "FlashAttention and Optimized Kernels" (programmer.ie), "The online
+ * softmax".
+ *
+ *  q     [B, H, N, d]    dtype       queries
+ *  k, v  [B, Hkv, N, d]  dtype       keys and values
+ *  o     [B, H, N, d]    dtype       output (written)
+ *  lse   [B, H, N]       float32     log-sum-exp per row (written; may be NULL)
+ *  scale                              score scale (1/sqrt(d) for standard attention)
+ *  dtype ATTN_BF16: d in {64, 128}; tcgen05 tensor-core kernel, fp32
+ *                   accumulation, P rounded to bf16 before P.V, O rounded
+ *                   to nearest-even bf16.
+ *        ATTN_F32:  d in {64, 128}; precise SIMT kernel: dot products and
+ *                   the softmax sums accumulated in fp64, exp in fp32.
+ *  B, H, Hkv, N >= 0; N == 0 or B == 0 or H == 0 is a no-op returning ATTN_OK.
+ */
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                       int B, int H, int Hkv, int N, int d, int causal, float scale,
+                       attn_dtype_t dtype, attn_stream_t stream);
+
+/*
+ * attn_decode_workspace_size -- bytes of device workspace attn_decode_paged
+ * needs for up to max_splits partial results per (sequence, query head):
+ * fp32 m and l [B, H, max_splits] and fp32 o~ [B, H, max_splits, d], each
+ * region 256-byte aligned.  Returns 0 for invalid arguments.
+ */
+size_t attn_decode_workspace_size(int B, int H, int d, int max_splits);
+
+/*
+ * attn_decode_paged -- one query token per sequence against a paged,
+ * ragged KV cache, split along the keys (split-KV / Flash-Decoding), then
+ * merged exactly.
+ *
+ * Follows "3.4 Attention Kernels", sections "Decode attention and
+ * Flash-Decoding" (split the cache into chunks, one partial (m_c, l_c, o~_c)
+ * per chunk, merged by the log-sum-exp merge in a small reduction kernel;
+ * all query heads of a GQA group share each loaded K/V tile) and "Paged and
+ * ragged layouts: FlashInfer" (the kernel gathers K/V through a page table).
+ *
+ *  q           [B, H, d]                   bf16   one query token per sequence
+ *  k_pages     [P, Hkv, page_size, d]      bf16   shared pool of K pages
+ *  v_pages     [P, Hkv, page_size, d]      bf16   shared pool of V pages
+ *  page_table  [B, max_pages_per_seq]      int32  page ids (< num_pages) of each sequence, in token order
+ *  kv_lens     [B]                         int32  tokens of each sequence, 0 <= kv_lens[b] <= max_pages_per_seq * page_size
+ *  o           [B, H, d]                   bf16   output (written)
+ *  lse         [B, H]                      fp32   log-sum-exp (written; may be NULL)
+ *  num_pages   P, the pool size (the tensor-map extent; page ids are not range-checked on the device)
+ *  num_splits  upper bound on the key chunks per sequence; <= 0 picks one from
+ *              B, Hkv, max_pages_per_seq and the SM count.  The chunk is
+ *              ceil(max_pages_per_seq / num_splits) pages; sequence b uses
+ *              ceil(pages_b / chunk) partials.  No device-to-host copy is made.
+ *  workspace   >= attn_decode_workspace_size(B, H, d, num_splits used) bytes;
+ *              with num_splits <= 0 pass the size for attn_decode_max_splits().
+ *  Supported: d == 128, page_size == 16, H / Hkv <= 16.  Results are
+ *  deterministic for a given num_splits.
+ */
+attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                                const int32_t *page_table, const int32_t *kv_lens, void *o, float *lse,
+                                int B, int H, int Hkv, int d, int page_size, int max_pages_per_seq,
+                                int num_pages, float scale, int num_splits,
+                                void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * attn_decode_max_splits -- the split count attn_decode_paged picks when
+ * called with num_splits <= 0 on the current device (for sizing the
+ * workspace).  Returns 0 for invalid arguments.
+ */
+int attn_decode_max_splits(int B, int H, int Hkv, int max_pages_per_seq);
+
+/*
+ * merge_partials -- exact merge of per-chunk partial results.
+ *
+ * Follows "3.4 Attention Kernels", section "Online softmax" (the merge of two
+ * partial results computed on disjoint key sets), applied over S partials:
+ * m = max_s m_s, l = sum_s exp(m_s - m) l_s, o~ = sum_s exp(m_s - m) o~_s,
+ * then O = o~ / l and LSE = m + ln l.  "FlashAttention and Optimized
+ * Kernels", "The decode shape: splitting the keys" names the operation.
+ * An empty partial is (m, l, o~) = (-inf, 0, 0) and contributes nothing.
+ *
+ *  m, l        [B, H, S]     fp32   per-partial running max (natural-log units of the
+ *                                   scaled scores) and denominator
+ *  o_tilde     [B, H, S, d]  fp32   per-partial unnormalised output
+ *  num_parts   [B]           int32  partials used for sequence b (first num_parts[b]
+ *                                   of S); NULL means all S
+ *  o           [B, H, d]     o_dtype  merged output (written)
+ *  lse         [B, H]        fp32   merged log-sum-exp (written; may be NULL)
+ *  d in {64, 128}; S >= 1.
+ */
+attn_status_t merge_partials(const float *m, const float *l, const float *o_tilde,
+                             const int32_t *num_parts, int B, int H, int S, int d,
+                             void *o, attn_dtype_t o_dtype, float *lse, attn_stream_t stream);
+
+/* attn_status_string -- a static, human-readable name for a status code. */
+const char *attn_status_string(attn_status_t status);
+
+/*
+ * attn_device_error -- read the device-wide error word of the current device
+ * (synchronises the device).  0 means no kernel has recorded a failure; a
+ * non-zero value is a bit set of ATTN_DEVERR_* codes.  clear != 0 resets it.
+ * Returns ATTN_ERR_CUDA if the read itself failed.
+ */
+attn_status_t attn_device_error(uint32_t *code, int clear);
+
+#define ATTN_DEVERR_WAIT_TIMEOUT 0x1u   /* a pipeline wait gave up after its iteration limit */
+#define ATTN_DEVERR_BAD_PAGE     0x2u   /* a page id outside [0, num_pages) was skipped */
+#define ATTN_DEVERR_TMEM_ALLOC   0x4u   /* tensor memory allocation returned an unusable address */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */
