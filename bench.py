@@ -124,6 +124,16 @@ class ClockSampler:
                 "samples": len(rows), "reasons": sorted(reasons)}
 
 
+def smi_index(local_rank: int) -> str:
+    """nvidia-smi's name for this rank's GPU (CUDA_VISIBLE_DEVICES entries are physical ids or UUIDs)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
 # ------------------------------------------------------------------ ncu traffic records
 
 def kernel_source_sha(files):
@@ -213,7 +223,7 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-PREFILL_SAMPLE = {"heads": [0, 9, 18, 27], "rows": 2048}
+PREFILL_SAMPLE = {"heads": [0, 4, 9, 13, 18, 22, 27, 31], "rows": 4096}
 DECODE_SAMPLE_SEQS = [0, 7, 21, 42]
 
 
@@ -235,30 +245,47 @@ def cpu_baseline(host, kv):
 
 # ------------------------------------------------------------------ the reference arm: the oracle on the host
 
+def bench_config(world, decode_desc):
+    from exact_tiled_attention_11_gb300 import workloads as W
+    return {
+        "workload": f"{W.C3.name} + {W.C4.name}",
+        "prefill": "attn_fwd bf16 causal B=1 H=32 Hkv=8 N=8192 d=128 scale=1/sqrt(128)",
+        "decode": decode_desc,
+        "l2": "no flush; every input set is larger than L2 (prefill 160 MiB touched, decode streams 4.1 GB per step)",
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+    }
+
+
 def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores, on bounded samples of the same workload."""
     if rank != 0:
         return 0
     import numpy as np
     from exact_tiled_attention_11_gb300 import workloads as W
     q, k, v = W.prefill_inputs_for(W.C3)
+    kv = W.decode_inputs_for(W.C4)
     rng = np.random.default_rng(0)
-    per_step_rows = 256
-    times, flops = [], []
+    per_step_rows = 1024
+    times, flops, dtimes, dbytes = [], [], [], []
     for i in range(args.warmup + args.steps):
         rows = np.sort(rng.choice(W.C3.N, per_step_rows, replace=False))
         fl, dt = oracle_prefill_sample(q, k, v, [i % W.C3.H], rows, W.C3.scale)
+        nb, ddt = oracle_decode_sample(kv, [i % W.C4.B], W.C4.scale)
         if i >= args.warmup:
             times.append(dt)
             flops.append(fl)
+            dtimes.append(ddt)
+            dbytes.append(nb)
     value = sum(flops) / sum(times) / 1e12
-    ms = 1e3 * sum(times) / len(times)
+    ms = 1e3 * (sum(times) + sum(dtimes)) / len(times)
     sample = (f"each step: float64 NumPy oracle on {per_step_rows} random query rows of one head of the "
-              f"N=8192 causal workload (one (b, h) slice; heads cycle per step)")
+              f"N=8192 causal prefill workload (heads cycle per step) and on one of the 64 decode sequences")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": W.C3.name, "parallelism": "host cores (oracle)"},
+        "config": bench_config(world, "attn_decode_paged workload, oracle gather + attention per sequence"),
+        "decode": {"value": sum(dbytes) / sum(dtimes) / 1e9, "unit": "GB/s"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -301,7 +328,7 @@ def run_ours(args, rank, local_rank, world):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local_rank) as clk:
+    with ClockSampler(smi_index(local_rank)) as clk:
         start = torch.cuda.Event(enable_timing=True)
         stop = torch.cuda.Event(enable_timing=True)
         start.record(stream)
@@ -398,14 +425,9 @@ def run_ours(args, rank, local_rank, world):
         "metric": METRIC, "value": pre_tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {
-            "workload": f"{W.C3.name} + {W.C4.name}",
-            "prefill": "attn_fwd bf16 causal B=1 H=32 Hkv=8 N=8192 d=128 scale=1/sqrt(128)",
-            "decode": (f"attn_decode_paged bf16 B=64 H=32 Hkv=8 d=128 page=16 lengths randint[512,32768] seed 0 "
-                       f"(pool {kv.k_pages.shape[0]} pages), auto split count {splits}"),
-            "l2": "no flush; every input set is larger than L2 (prefill 160 MiB touched, decode streams 4.1 GB per step)",
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-        },
+        "config": bench_config(world, (f"attn_decode_paged bf16 B=64 H=32 Hkv=8 d=128 page=16 lengths "
+                                       f"randint[512,32768] seed 0 (pool {kv.k_pages.shape[0]} pages), "
+                                       f"auto split count {splits}")),
         "decode": {"value": dec_gbs, "unit": "GB/s", "frac_of_hbm": dec_gbs / hbm_peak,
                    "ms_per_call": dec_tot / args.steps},
         "prefill": {"value": pre_tflops, "unit": "TFLOP/s", "frac_of_bf16": pre_tflops / t_peak,
@@ -422,6 +444,33 @@ def run_ours(args, rank, local_rank, world):
     return 0
 
 
+def run_profile_case(args):
+    """One kernel family alone, for ncu: W warm-up launches then one more launch.
+
+    prefill: the long causal workload (B=1, H=32, Hkv=8, N=8192, d=128).
+    decode:  the paged decode workload restricted to its first --decode-batch
+             sequences (same length distribution and page placement recipe).
+    """
+    import torch
+    import exact_tiled_attention_11_gb300 as lib
+    from exact_tiled_attention_11_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    lib.load_library()
+    if args.profile == "prefill":
+        q, k, v = (t.to(dev) for t in W.prefill_inputs_for(W.C3))
+        for _ in range(args.warmup + 1):
+            lib.attn_fwd(q, k, v, causal=True, scale=W.C3.scale)
+    else:
+        kv = W.decode_inputs_for(W.C4, B=args.decode_batch)
+        t = [x.to(dev) for x in (kv.q, kv.k_pages, kv.v_pages, kv.page_table, kv.kv_lens)]
+        for _ in range(args.warmup + 1):
+            lib.attn_decode_paged(*t, scale=W.C4.scale, num_splits=0)
+        print(f"decode case: {args.decode_batch} sequences, {decode_bytes(kv)} algorithmic bytes per call")
+    torch.cuda.synchronize()
+    assert lib.attn_device_error() == 0
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -429,7 +478,12 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+                    help="run one kernel family alone (for ncu) instead of the benchmark")
+    ap.add_argument("--decode-batch", type=int, default=16)
     args = ap.parse_args(argv)
+    if args.profile:
+        return run_profile_case(args)
     args.warmup = max(args.warmup, 3)
     rank, local_rank, world = dist_env()
     if world > 1:
