@@ -10,6 +10,7 @@ from ._lib import (  # noqa: F401
     AttnError,
     attn_decode_max_splits,
     attn_decode_paged,
+    attn_decode_paged_noalloc,
     attn_decode_workspace_size,
     attn_device_error,
     attn_fwd,

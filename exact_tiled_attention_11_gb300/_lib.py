@@ -56,6 +56,9 @@ def load_library() -> ctypes.CDLL:
         lib.attn_decode_paged.restype = i32
         lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32,
                                           vp, sz, vp]
+        lib.attn_decode_paged_noalloc.restype = i32
+        lib.attn_decode_paged_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
+                                                  i32, vp]
         lib.merge_partials.restype = i32
         lib.merge_partials.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, i32, vp, vp]
         lib.attn_status_string.restype = ctypes.c_char_p
@@ -158,6 +161,28 @@ def attn_decode_paged(q, k_pages, v_pages, page_table, kv_lens, o=None, lse=None
         _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens), _ptr(o), _ptr(lse),
         B, H, Hkv, d, ps, maxp, P, (1.0 / d ** 0.5) if scale is None else float(scale), int(num_splits),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream, q.device)))
+    return o, lse
+
+
+def attn_decode_paged_noalloc(q, k_pages, v_pages, page_table, kv_lens, o, lse, *, scale=None, num_splits=0,
+                              stream=None):
+    """attn_decode_paged with the library's fixed device scratch array instead of a
+    workspace, for callers that cannot allocate device memory.  ``o`` [B, H, d] bf16
+    and ``lse`` [B, H] fp32 must be given; nothing is allocated."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(kv_lens, "kv_lens", torch.int32, 1)
+    _need(o, "o", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    B, H, d = q.shape
+    P, Hkv, ps, _ = k_pages.shape
+    _check("attn_decode_paged_noalloc", lib.attn_decode_paged_noalloc(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens), _ptr(o), _ptr(lse),
+        B, H, Hkv, d, ps, page_table.shape[1], P, (1.0 / d ** 0.5) if scale is None else float(scale),
+        int(num_splits), _stream(stream, q.device)))
     return o, lse
 
 

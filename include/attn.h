@@ -150,6 +150,38 @@ attn_status_t merge_partials(const float *m, const float *l, const float *o_tild
                              const int32_t *num_parts, int B, int H, int S, int d,
                              void *o, attn_dtype_t o_dtype, float *lse, attn_stream_t stream);
 
+/*
+ * attn_decode_paged_noalloc -- attn_decode_paged for callers that cannot
+ * allocate device memory.  The pages this library follows have no
+ * counterpart to it; it exists for callers such as a plugin or custom op
+ * inside another runtime that is handed only its input and output buffers
+ * (no allocator, no workspace), or a latency-critical serving loop that must
+ * not call cudaMalloc because it can synchronise the device.
+ *
+ * Arguments, layouts, results and errors are those of attn_decode_paged,
+ * without workspace and workspace_bytes: the per-chunk partials go to a fixed
+ * array in device global memory that belongs to this library,
+ * ATTN_DECODE_NOALLOC_SCRATCH_BYTES long, which every GPU that loads the
+ * library holds until the process exits.  A request whose partials,
+ * attn_decode_workspace_size(B, H, d, splits used), exceed that size returns
+ * ATTN_ERR_WORKSPACE before anything is launched (with num_splits <= 0 the
+ * automatic split count decides the size; pass a smaller num_splits to fit).
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, with the caller's current device); make that
+ * first call before any stream capture.  All calls on a device share the one
+ * array and it keeps the previous call's contents; nothing in it needs to
+ * start at zero, because every partial the merge reads is written earlier in
+ * the same call.  Calls that overlap on the GPU (on different streams, or
+ * from several host threads without ordering) race on the array: order them.
+ */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (40u * 1024u * 1024u)
+attn_status_t attn_decode_paged_noalloc(const void *q, const void *k_pages, const void *v_pages,
+                                        const int32_t *page_table, const int32_t *kv_lens, void *o, float *lse,
+                                        int B, int H, int Hkv, int d, int page_size, int max_pages_per_seq,
+                                        int num_pages, float scale, int num_splits, attn_stream_t stream);
+
 /* attn_status_string -- a static, human-readable name for a status code. */
 const char *attn_status_string(attn_status_t status);
 
