@@ -9,26 +9,29 @@
 // masking only key tiles j <= i are visited and the diagonal tile is masked.
 //
 // GB300 mapping: one CTA per PAIR of 128-row query tiles (A and B) of one
-// (batch, head), 384 threads, one CTA per SM.  The two tiles form two
-// independent chains  S_c(j) -> softmax_c(j) -> P_c(j) -> O_c += P_c(j) V_j ->
-// S_c(j+1) ... and the tensor core alternates between them, so that the
-// softmax of one tile runs while the MMAs of the other tile execute (the
-// FlashAttention-3 overlap, here with tcgen05 and tensor memory).
-//   warp 0      TMA producer: Q_A, Q_B once, then K_j / V_j into 2-stage rings
-//               (128-byte-swizzled tiles, completion on mbarriers).
-//   warps 1, 2  one MMA warp per chain (warp 1 also allocates tensor memory):
-//                 S_c = Q_c K_j^T  (SS form; Q, K K-major in SMEM)
-//                 O_c += P_c V_j   (TS form; P from TMEM, V MN-major in SMEM)
-//               issued by an elected lane of the converged warp, completion
-//               tracked by tcgen05.commit on mbarriers.  Two issuing warps
-//               keep the tensor core fed while each waits on its own chain.
+// (batch, head), 384 threads, one CTA per SM.  Each tile is a chain
+//     S_c(j) = Q_c K_j^T -> softmax_c(j) -> P_c(j) -> O_c += P_c(j) V_j
+// and, because P lives in shared memory rather than over S, S_c(j+1) can be
+// computed as soon as softmax has loaded S_c(j) into registers: the tensor
+// core works on the next score tile (and on the other chain) while the
+// exponentials of this one are evaluated (the FlashAttention-3 overlap, here
+// with tcgen05, tensor memory and TMA).
+//   warp 0      TMA: Q_A, Q_B once, then K_j into a 2-stage ring
+//   warp 2      TMA: V_j into a single stage (it is needed only after softmax)
+//   warp 1      allocates tensor memory and issues every MMA from an elected
+//               lane of the converged warp, polling both chains and issuing
+//               whichever next MMA is ready:
+//                 S_c = Q_c K_j^T  (SS; Q, K K-major in SMEM; D in TMEM)
+//                 O_c += P_c V_j   (SS; P K-major, V MN-major in SMEM; D in TMEM)
+//               completion tracked by tcgen05.commit on mbarriers.
 //   warps 4-7   softmax warpgroup of tile A, warps 8-11 of tile B; one thread
-//               per query row (= TMEM lane): load S, mask, row max, p = 2^(s'-m),
-//               row sum, write P = bf16(p) over the first 64 columns of S,
-//               rescale O in TMEM lazily (the reference maximum moves only
-//               when the row max outgrows it by more than 2^8; the result does
-//               not depend on the reference, and p stays <= 256), and at the
-//               end write O = o~ / l (bf16, round to nearest even) and the LSE.
+//               per query row (= TMEM lane): load S, release it, mask, row
+//               max, p = 2^(s' - m), row sum, write P = bf16(p) (round to
+//               nearest even) to shared memory in the 128-byte-swizzled
+//               K-major layout, rescale O in TMEM lazily (the reference
+//               maximum moves only when the row max outgrows it by more than
+//               2^8; the result does not depend on the reference, and p stays
+//               <= 256), and at the end write O = o~ / l and the LSE.
 // Tensor memory, 512 columns: S_A [0,128), S_B [128,256), O_A [256,256+d),
 // O_B [384,384+d).  Query-tile pairs are ordered heaviest causal pair first.
 #include <algorithm>
@@ -43,7 +46,6 @@ namespace {
 constexpr int BM = 128;      // query rows per tile (= TMEM lanes)
 constexpr int BN = 128;      // keys per K/V tile
 constexpr int kKStages = 2;
-constexpr int kVStages = 2;
 constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -54,11 +56,12 @@ struct PrefillSmem {
   static constexpr int kTileBytes = BN * D * 2;
   alignas(1024) uint8_t q[2][BM * D * 2];
   alignas(1024) uint8_t k[kKStages][kTileBytes];
-  alignas(1024) uint8_t v[kVStages][kTileBytes];
+  alignas(1024) uint8_t v[kTileBytes];
+  alignas(1024) uint8_t p[2][BM * BN * 2];  // P_A, P_B: 128 rows x 128 keys bf16, two 64-key swizzled boxes
   uint64_t q_full;
   uint64_t k_full[kKStages], k_empty[kKStages];
-  uint64_t v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t v_full, v_empty;
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -94,6 +97,19 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // One lane of a converged warp (the MMA instructions are issued by it while
 // the whole warp runs the control flow, so their operands stay warp-uniform).
 __device__ __forceinline__ bool elect_one() {
@@ -104,6 +120,15 @@ __device__ __forceinline__ bool elect_one() {
       "selp.u32 %0, 1, 0, P;\n\t}"
       : "=r"(pred));
   return pred != 0;
+}
+
+// Generic-proxy shared-memory writes made visible to the tensor core (async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // Scale a 32-column chunk of O (one row per thread) in tensor memory.
@@ -152,21 +177,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm.q_full), 1);
-    // a stage is handed back once both chains' MMAs have read it
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(smem_u32(&sm.k_full[s]), 1);
-      mbar_init(smem_u32(&sm.k_empty[s]), 2);
+      mbar_init(smem_u32(&sm.k_empty[s]), 1);
     }
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_init(smem_u32(&sm.v_full[s]), 1);
-      mbar_init(smem_u32(&sm.v_empty[s]), 2);
-    }
+    mbar_init(smem_u32(&sm.v_full), 1);
+    mbar_init(smem_u32(&sm.v_empty), 1);
     for (int c = 0; c < 2; ++c) {
       mbar_init(smem_u32(&sm.s_full[c]), 1);
+      mbar_init(smem_u32(&sm.s_free[c]), 128);
       mbar_init(smem_u32(&sm.p_full[c]), 128);
       mbar_init(smem_u32(&sm.pv_done[c]), 1);
     }
-    mbar_init(smem_u32(&sm.mma_done), 2);
+    mbar_init(smem_u32(&sm.mma_done), 1);
     sm.abort = 0;
     fence_barrier_init();
   }
@@ -180,17 +203,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
 
   // Register split: the CTA is launched with 384 threads x 168 registers =
-  // 64,512.  Warpgroup 0 (producer, MMA issuer, two idle warps) gives up to
+  // 64,512.  Warpgroup 0 (TMA warps, MMA warp, one idle warp) gives up to
   // 56 per thread and the two softmax warpgroups take 224:
   // 128 x 56 + 256 x 224 = 64,512, exactly the launch's allocation.
   if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
   if (warp == 0) {
-    // ================================================================ TMA producer
+    // ================================================================ TMA: Q and K
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      const uint64_t keep = l2_policy_evict_last();    // K/V tiles are re-read by other query tiles
+      const uint64_t keep = l2_policy_evict_last();    // K tiles are re-read by other query tiles
       const uint64_t once = l2_policy_evict_first();   // each Q tile is read once
       const uint32_t qbar = smem_u32(&sm.q_full);
       mbar_arrive_expect_tx(qbar, (has_b ? 2 : 1) * BM * D * 2);
@@ -198,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int x = 0; x < D / 64; ++x)
           tma_load_3d_hint(smem_u32(sm.q[c]) + x * kBoxBytes, &tm_q, qbar, x * 64, row0[c], b * H + h, once);
-      int k_issued = 0, v_issued = 0;
+      int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int ks = j % kKStages;
         if (j >= kKStages && !mbar_wait(smem_u32(&sm.k_empty[ks]), ((j / kKStages) - 1) & 1, &sm.abort)) break;
@@ -207,79 +229,122 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int x = 0; x < D / 64; ++x)
           tma_load_3d_hint(smem_u32(sm.k[ks]) + x * kBoxBytes, &tm_k, kbar, x * 64, j * BN, b * Hkv + kvh, keep);
-        ++k_issued;
-        const int vs = j % kVStages;
-        if (j >= kVStages && !mbar_wait(smem_u32(&sm.v_empty[vs]), ((j / kVStages) - 1) & 1, &sm.abort)) break;
-        const uint32_t vbar = smem_u32(&sm.v_full[vs]);
-        mbar_arrive_expect_tx(vbar, Smem::kTileBytes);
-#pragma unroll
-        for (int x = 0; x < D / 64; ++x)
-          tma_load_3d_hint(smem_u32(sm.v[vs]) + x * kBoxBytes, &tm_v, vbar, x * 64, j * BN, b * Hkv + kvh, keep);
-        ++v_issued;
+        ++issued;
       }
       // drain: every issued copy must land before the CTA's shared memory is released
       mbar_wait(qbar, 0, nullptr);
-      for (int s = 0; s < kKStages && s < k_issued; ++s) {
-        const int last = s + ((k_issued - 1 - s) / kKStages) * kKStages;
+      for (int s = 0; s < kKStages && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / kKStages) * kKStages;
         mbar_wait(smem_u32(&sm.k_full[s]), (last / kKStages) & 1, nullptr);
-      }
-      for (int s = 0; s < kVStages && s < v_issued; ++s) {
-        const int last = s + ((v_issued - 1 - s) / kVStages) * kVStages;
-        mbar_wait(smem_u32(&sm.v_full[s]), (last / kVStages) & 1, nullptr);
       }
     }
     __syncwarp();
-  } else if (warp == 1 || warp == 2) {
-    // ================================================================ MMA warps, one per chain
-    const int c = warp - 1;
-    const int n_c = n_tiles[c];
+  } else if (warp == 2) {
+    // ================================================================ TMA: V (single stage)
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_v);
+      const uint64_t keep = l2_policy_evict_last();
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        if (j >= 1 && !mbar_wait(smem_u32(&sm.v_empty), (j - 1) & 1, &sm.abort)) break;
+        const uint32_t vbar = smem_u32(&sm.v_full);
+        mbar_arrive_expect_tx(vbar, Smem::kTileBytes);
+#pragma unroll
+        for (int x = 0; x < D / 64; ++x)
+          tma_load_3d_hint(smem_u32(sm.v) + x * kBoxBytes, &tm_v, vbar, x * 64, j * BN, b * Hkv + kvh, keep);
+        ++issued;
+      }
+      if (issued > 0) mbar_wait(smem_u32(&sm.v_full), (issued - 1) & 1, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================================================================ MMA warp (polls both chains)
     constexpr uint32_t idesc_qk = tc05::idesc_bf16_f32(BM, BN, false);
     constexpr uint32_t idesc_pv = tc05::idesc_bf16_f32(BM, D, true);
-    const uint32_t q_addr = smem_u32(sm.q[c]);
-    const uint32_t s_tmem = tmem + c * BN;
-    const uint32_t o_tmem = tmem + 2 * BN + c * BN;
-    // key tiles the other chain does not visit are handed back with two arrivals from this chain
-    const int n_other = n_tiles[1 - c];
+    int qk_next[2] = {0, 0};    // next S_c(j) to issue
+    int pv_next[2] = {0, 0};    // next O_c += P_c(j) V_j to issue
+    int k_rel = 0, v_rel = 0;   // next K stage / V tile to hand back to the producers
     bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.q_full), 0, &sm.abort));
-    for (int j = 0; ok && j < n_c; ++j) {
-      // S_c(j) = Q_c K_j^T, once O_c += P_c(j-1) V_{j-1} has completed (S_c holds P_c(j-1))
-      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.pv_done[c]), (j - 1) & 1, &sm.abort))) break;
-      const int ks = j % kKStages;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.k_full[ks]), (j / kKStages) & 1, &sm.abort))) break;
-      tc05::fence_after_sync();
-      const uint32_t k_addr = smem_u32(sm.k[ks]);
+    tc05::fence_after_sync();
+    unsigned long long t_idle = 0;
+    uint32_t spins = 0;
+    // lane 0's view of a barrier phase, shared so that the warp stays converged
+    auto ready = [&](uint64_t *bar, uint32_t parity) -> bool {
+      return __shfl_sync(0xffffffffu, mbar_test(smem_u32(bar), parity) ? 1 : 0, 0) != 0;
+    };
+    while (ok && (pv_next[0] < n_tiles[0] || pv_next[1] < n_tiles[1])) {
+      bool progressed = false;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-        const uint64_t da = tc05::sdesc_sw128(q_addr + off, 16, 1024);
-        const uint64_t db = tc05::sdesc_sw128(k_addr + off, 16, 1024);
-        if (elect_one()) tc05::mma_ss(s_tmem, da, db, idesc_qk, kk > 0);
-        __syncwarp();
-      }
-      if (elect_one()) {
-        tc05::commit(smem_u32(&sm.s_full[c]));
-        tc05::commit(smem_u32(&sm.k_empty[ks]));
-        if (j >= n_other) tc05::commit(smem_u32(&sm.k_empty[ks]));
-      }
-      __syncwarp();
-      // O_c += P_c(j) V_j, once softmax has written P_c(j)
-      const int vs = j % kVStages;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_full[c]), j & 1, &sm.abort))) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.v_full[vs]), (j / kVStages) & 1, &sm.abort))) break;
-      tc05::fence_after_sync();
-      const uint32_t v_addr = smem_u32(sm.v[vs]);
+      for (int c = 0; c < 2; ++c) {
+        // S_c(j) = Q_c K_j^T, once softmax has taken S_c(j-1) out of tensor memory
+        const int jq = qk_next[c];
+        if (jq < n_tiles[c] && (jq == 0 || ready(&sm.s_free[c], (jq - 1) & 1)) &&
+            ready(&sm.k_full[jq % kKStages], (jq / kKStages) & 1)) {
+          tc05::fence_after_sync();
+          const uint32_t q_addr = smem_u32(sm.q[c]);
+          const uint32_t k_addr = smem_u32(sm.k[jq % kKStages]);
 #pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk) {
-        const uint64_t db = tc05::sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024);
-        if (elect_one()) tc05::mma_ts(o_tmem, s_tmem + kk * 8, db, idesc_pv, (j > 0) || (kk > 0));
-        __syncwarp();
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            const uint64_t da = tc05::sdesc_sw128(q_addr + off, 16, 1024);
+            const uint64_t db = tc05::sdesc_sw128(k_addr + off, 16, 1024);
+            if (elect_one()) tc05::mma_ss(tmem + c * BN, da, db, idesc_qk, kk > 0);
+            __syncwarp();
+          }
+          if (elect_one()) tc05::commit(smem_u32(&sm.s_full[c]));
+          __syncwarp();
+          qk_next[c] = jq + 1;
+          progressed = true;
+          // hand back K stages whose every reader has been issued
+          while (k_rel < n_kv && (qk_next[0] > k_rel || k_rel >= n_tiles[0]) &&
+                 (qk_next[1] > k_rel || k_rel >= n_tiles[1])) {
+            if (elect_one()) tc05::commit(smem_u32(&sm.k_empty[k_rel % kKStages]));
+            __syncwarp();
+            ++k_rel;
+          }
+        }
+        // O_c += P_c(j) V_j, once softmax has written P_c(j) and V_j has landed
+        const int jp = pv_next[c];
+        if (jp < qk_next[c] && ready(&sm.p_full[c], jp & 1) && ready(&sm.v_full, jp & 1)) {
+          tc05::fence_after_sync();
+          const uint32_t p_addr = smem_u32(sm.p[c]);
+          const uint32_t v_addr = smem_u32(sm.v);
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t da = tc05::sdesc_sw128(p_addr + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
+            const uint64_t db = tc05::sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024);
+            if (elect_one()) tc05::mma_ss(tmem + 2 * BN + c * BN, da, db, idesc_pv, (jp > 0) || (kk > 0));
+            __syncwarp();
+          }
+          if (elect_one()) tc05::commit(smem_u32(&sm.pv_done[c]));
+          __syncwarp();
+          pv_next[c] = jp + 1;
+          progressed = true;
+          while (v_rel < n_kv && (pv_next[0] > v_rel || v_rel >= n_tiles[0]) &&
+                 (pv_next[1] > v_rel || v_rel >= n_tiles[1])) {
+            if (elect_one()) tc05::commit(smem_u32(&sm.v_empty));
+            __syncwarp();
+            ++v_rel;
+          }
+        }
       }
-      if (elect_one()) {
-        tc05::commit(smem_u32(&sm.pv_done[c]));
-        tc05::commit(smem_u32(&sm.v_empty[vs]));
-        if (j >= n_other) tc05::commit(smem_u32(&sm.v_empty[vs]));
+      if (progressed) {
+        spins = 0;
+        t_idle = 0;
+      } else if ((++spins & 255u) == 0u) {
+        // nothing ready for a while: give up after the wait limit, or if another warp did
+        const unsigned long long now = global_timer_ns();
+        if (t_idle == 0) t_idle = now;
+        const bool aborted = *reinterpret_cast<volatile int *>(&sm.abort) != 0;
+        const bool expired = now - t_idle > kWaitLimitNs;
+        if (__shfl_sync(0xffffffffu, (aborted || expired) ? 1 : 0, 0)) {
+          if (lane == 0 && expired && !aborted) {
+            record_device_error(ATTN_DEVERR_WAIT_TIMEOUT);
+            sm.abort = 1;
+          }
+          ok = false;
+        }
       }
-      __syncwarp();
     }
     // every MMA this warp issued must complete before tensor memory is released
     if (elect_one()) tc05::commit(smem_u32(&sm.mma_done));
@@ -296,7 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_addr = tmem + lane_addr + c * BN;
     const uint32_t o_addr = tmem + lane_addr + 2 * BN + c * BN;
-    const int lim = causal ? min(q_row + 1, N) : N;  // keys [0, lim) are attended by this row
+    const uint32_t p_row = smem_u32(sm.p[c]) + row * 128;  // this row in each 64-key swizzled box
+    const int lim = causal ? min(q_row + 1, N) : N;        // keys [0, lim) are attended by this row
     const uint64_t scale2 = f2(scale_log2, scale_log2);
     float m_ref = -INFINITY;  // reference maximum (log2 units) that p and o~ are relative to
     float l = 0.f;
@@ -313,6 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q4 = 0; q4 < 4; ++q4) tc05::tmem_ld_x32(s_addr + q4 * 32, sr[q4]);
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) tc05::tmem_ld_wait(sr[q4]);
+      // S_c is in registers: the MMA warp may compute S_c(j+1) into it now
+      tc05::fence_before_sync();
+      mbar_arrive(smem_u32(&sm.s_free[c]));
 
       const int kv0 = j * BN;
       if (kv0 + BN > lim) {  // diagonal tile or ragged tail: mask keys >= lim
@@ -354,24 +423,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           pr[q4 >> 1][(q4 & 1) * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
         }
       }
-      tc05::tmem_st_x32(s_addr, pr[0]);
-      tc05::tmem_st_x32(s_addr + 32, pr[1]);
       float sum_lo, sum_hi;
       f2_split(add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3])), sum_lo, sum_hi);
       l = l * corr + (sum_lo + sum_hi);
 
-      if (__any_sync(0xffffffffu, move) && j > 0) {
-        // o~ must hold the complete P_{j-1} V_{j-1} before it is rescaled; the MMA
-        // issuer only started S_c(j) after that product completed, so this wait
-        // returns at once
+      // P_c(j-1) V_{j-1} must have completed: it reads the P buffer written below
+      // and o~ is rescaled in place
+      if (j > 0) {
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.pv_done[c]), (j - 1) & 1, &sm.abort))) {
           ok = false;
           break;
         }
         tc05::fence_after_sync();
+        if (__any_sync(0xffffffffu, move)) {
 #pragma unroll
-        for (int q4 = 0; q4 < D / 32; ++q4) rescale_o_chunk(o_addr + q4 * 32, corr);
+          for (int q4 = 0; q4 < D / 32; ++q4) rescale_o_chunk(o_addr + q4 * 32, corr);
+        }
       }
+      // P row -> shared memory: keys 64x + 8ch .. +7 at chunk ch of box x, chunk index XOR (row mod 8)
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          st_shared_v4(p_row + x * kBoxBytes + (((ch ^ row) & 7) << 4), pr[x][4 * ch], pr[x][4 * ch + 1],
+                       pr[x][4 * ch + 2], pr[x][4 * ch + 3]);
+      fence_proxy_async_smem();
       tc05::tmem_wait_st();
       tc05::fence_before_sync();
       mbar_arrive(smem_u32(&sm.p_full[c]));
