@@ -54,12 +54,13 @@ int device_sm_count() {
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
-// Split-KV plan from arguments only (no device-to-host copy): enough
-// (sequence, KV head, chunk) CTAs for ~6 per SM when every sequence is as long
-// as the longest, chunks of at most 64 and at least 8 pages.
+// Split-KV plan from arguments only (no device-to-host copy): chunks of at
+// most 128 pages (2 MiB of K/V per CTA at d = 128, long enough to amortise a
+// CTA's set-up), more splits when that gives fewer than ~6 CTAs per SM with
+// every sequence as long as the longest, and chunks of at least 8 pages.
 int auto_splits(int B, int Hkv, int max_pages, int num_sms) {
   const int want_ctas = 6 * std::max(num_sms, 1);
-  int s = ceil_div(max_pages, 64);
+  int s = ceil_div(max_pages, 128);
   s = std::max(s, ceil_div(want_ctas, static_cast<long long>(B) * Hkv));
   s = std::min(s, ceil_div(max_pages, 8));
   return std::max(s, 1);

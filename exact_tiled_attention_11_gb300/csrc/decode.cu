@@ -115,33 +115,56 @@ __global__ void __launch_bounds__(kThreads)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
+    // The warp reads the chunk's page ids 32 at a time (one coalesced load,
+    // the next batch fetched while the current one is issued); lane 0 issues
+    // the TMA copies.
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const uint64_t policy = l2_policy_evict_first();
-      const int32_t *row = page_table + static_cast<size_t>(b) * max_pages + first;
-      int issued = 0;
-      for (int i = 0; i < npg; ++i) {
-        const int s = i % kStages;
-        if (i >= kStages && !mbar_wait(smem_u32(&sm.empty[s]), ((i / kStages) - 1) & 1, &sm.abort)) break;
-        int page = row[i];
-        if (page < 0 || page >= num_pages) {
-          // out of the pool: TMA fills an out-of-range box with zeros; record it
-          record_device_error(ATTN_DEVERR_BAD_PAGE);
+    }
+    const uint64_t policy = l2_policy_evict_first();
+    const int32_t *row = page_table + static_cast<size_t>(b) * max_pages + first;
+    int issued = 0;
+    bool ok = true;
+    int next_ids = lane < npg ? row[lane] : 0;
+    for (int base = 0; ok && base < npg; base += 32) {
+      const int ids = next_ids;
+      if (base + 32 < npg) next_ids = (base + 32 + lane < npg) ? row[base + 32 + lane] : 0;
+      const int n = min(32, npg - base);
+      for (int t = 0; t < n; ++t) {
+        const int i = base + t;
+        const int page = __shfl_sync(0xffffffffu, ids, t);
+        int good = 1;
+        if (lane == 0) {
+          const int s = i % kStages;
+          if (i >= kStages && !mbar_wait(smem_u32(&sm.empty[s]), ((i / kStages) - 1) & 1, &sm.abort)) {
+            good = 0;
+          } else {
+            if (page < 0 || page >= num_pages) {
+              // out of the pool: TMA fills an out-of-range box with zeros; record it
+              record_device_error(ATTN_DEVERR_BAD_PAGE);
+            }
+            const int c2 = page * Hkv + kvh;
+            const uint32_t bar = smem_u32(&sm.full[s]);
+            const uint32_t dst = smem_u32(&sm.stage[s][0]);
+            mbar_arrive_expect_tx(bar, kStageBytes);
+            tma_load_3d_hint(dst, &tm_k, bar, 0, 0, c2, policy);
+            tma_load_3d_hint(dst + kHalfBytes, &tm_k, bar, 64, 0, c2, policy);
+            tma_load_3d_hint(dst + kPageBytes, &tm_v, bar, 0, 0, c2, policy);
+            tma_load_3d_hint(dst + kPageBytes + kHalfBytes, &tm_v, bar, 64, 0, c2, policy);
+            ++issued;
+          }
         }
-        const int c2 = page * Hkv + kvh;
-        const uint32_t bar = smem_u32(&sm.full[s]);
-        const uint32_t dst = smem_u32(&sm.stage[s][0]);
-        mbar_arrive_expect_tx(bar, kStageBytes);
-        tma_load_3d_hint(dst, &tm_k, bar, 0, 0, c2, policy);
-        tma_load_3d_hint(dst + kHalfBytes, &tm_k, bar, 64, 0, c2, policy);
-        tma_load_3d_hint(dst + kPageBytes, &tm_v, bar, 0, 0, c2, policy);
-        tma_load_3d_hint(dst + kPageBytes + kHalfBytes, &tm_v, bar, 64, 0, c2, policy);
-        ++issued;
+        if (!__shfl_sync(0xffffffffu, good, 0)) {
+          ok = false;
+          break;
+        }
       }
-      // Teardown: the ring is reused as merge scratch, and the CTA may exit
-      // early, only after every issued copy has landed.  Wait (bounded) for
-      // the last phase of each stage this thread armed.
+    }
+    // Teardown: the ring is reused as merge scratch, and the CTA may exit
+    // early, only after every issued copy has landed.  Wait (bounded) for
+    // the last phase of each stage this thread armed.
+    if (lane == 0) {
       for (int s = 0; s < kStages && s < issued; ++s) {
         const int last_i = s + ((issued - 1 - s) / kStages) * kStages;
         mbar_wait(smem_u32(&sm.full[s]), (last_i / kStages) & 1, nullptr);
@@ -365,22 +388,34 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int j = 0; j < E; ++j) o[j] = 0.f;
   if (m != -INFINITY) {
-    for (int s = 0; s < n; ++s) {
-      const float ms = m_in[base + s];
-      if (ms == -INFINITY) continue;  // empty partial
-      const float w = expf(ms - m);
-      l += w * l_in[base + s];
-      const float *src = o_in + (base + s) * D + lane * E;
-      if constexpr (E == 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(src);
-        o[0] += w * v.x;
-        o[1] += w * v.y;
-        o[2] += w * v.z;
-        o[3] += w * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2 *>(src);
-        o[0] += w * v.x;
-        o[1] += w * v.y;
+    // four partials per step: their loads are independent and overlap
+    for (int s0 = 0; s0 < n; s0 += 4) {
+      float w[4], lv[4], ov[4][E];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int s = s0 + u;
+        const bool in = s < n;
+        const float ms = in ? m_in[base + s] : -INFINITY;
+        lv[u] = in ? l_in[base + s] : 0.f;
+        const float *src = o_in + (base + (in ? s : 0)) * D + lane * E;
+        if constexpr (E == 4) {
+          const float4 v = *reinterpret_cast<const float4 *>(src);
+          ov[u][0] = v.x;
+          ov[u][1] = v.y;
+          ov[u][2] = v.z;
+          ov[u][3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2 *>(src);
+          ov[u][0] = v.x;
+          ov[u][1] = v.y;
+        }
+        w[u] = (ms == -INFINITY) ? 0.f : expf(ms - m);  // an empty partial weighs nothing
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        l += w[u] * lv[u];
+#pragma unroll
+        for (int j = 0; j < E; ++j) o[j] += w[u] * ov[u][j];
       }
     }
   }
