@@ -104,7 +104,9 @@ size_t attn_decode_workspace_size(int B, int H, int d, int max_splits);
  *  kv_lens     [B]                         int32  tokens of each sequence, 0 <= kv_lens[b] <= max_pages_per_seq * page_size
  *  o           [B, H, d]                   bf16   output (written)
  *  lse         [B, H]                      fp32   log-sum-exp (written; may be NULL)
- *  num_pages   P, the pool size (the tensor-map extent; page ids are not range-checked on the device)
+ *  num_pages   P, the pool size (the tensor-map extent).  A page id outside [0, P)
+ *              reads as zeros (TMA fills out-of-range boxes) and is recorded as
+ *              ATTN_DEVERR_BAD_PAGE; so is a kv_lens value beyond the table.
  *  num_splits  upper bound on the key chunks per sequence; <= 0 picks one from
  *              B, Hkv, max_pages_per_seq and the SM count.  The chunk is
  *              ceil(max_pages_per_seq / num_splits) pages; sequence b uses
