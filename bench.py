@@ -191,6 +191,53 @@ def decode_bytes(kv):
     return kv.kv_bytes() + kv.q.numel() * 2 + pages_used * 4 + B * 4 + B * H * d * 2 + B * H * 4
 
 
+# ------------------------------------------------------------------ launch overhead (eager vs CUDA graph)
+
+def launch_overhead(dev, calls=20, reps=20):
+    """Wall time per attn_decode_paged call on a launch-bound problem (one sequence of
+    16 tokens, H=32, Hkv=8): issued eagerly through the binding, and replayed from a
+    CUDA graph that captured `calls` back-to-back calls (one decode step of a
+    `calls`-layer model).  Measured apart from the benchmark's timed region."""
+    import torch
+    import exact_tiled_attention_11_gb300 as lib
+    from exact_tiled_attention_11_gb300 import workloads as W
+    kv = W.decode_inputs(1, 32, 8, 128, 16, 16, 16, seed=5)
+    t = [x.to(dev) for x in (kv.q, kv.k_pages, kv.v_pages, kv.page_table, kv.kv_lens)]
+    S = lib.attn_decode_max_splits(1, 32, 8, kv.max_pages)
+    ws = torch.empty(lib.attn_decode_workspace_size(1, 32, 128, S), dtype=torch.uint8, device=dev)
+    o = torch.empty(1, 32, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(1, 32, dtype=torch.float32, device=dev)
+
+    def call():
+        lib.attn_decode_paged(*t, o, lse, num_splits=S, workspace=ws)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(5):
+            call()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(calls * reps):
+        call()
+    torch.cuda.synchronize(dev)
+    eager_us = (time.perf_counter() - t0) / (calls * reps) * 1e6
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(calls):
+            call()
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    graph_us = (time.perf_counter() - t0) / (calls * reps) * 1e6
+    return {"workload": "attn_decode_paged, 1 sequence x 16 tokens, H=32 Hkv=8 d=128 (2 kernels per call)",
+            "eager_us_per_call": eager_us, "graph_us_per_call": graph_us, "calls_per_graph": calls}
+
+
 # ------------------------------------------------------------------ CPU oracle legs
 
 def oracle_prefill_sample(q, k, v, heads, rows, scale):
@@ -438,6 +485,7 @@ def run_ours(args, rank, local_rank, world):
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
+    line["launch_overhead"] = launch_overhead(dev)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(host, kv)
     print(json.dumps(line), flush=True)
