@@ -8,12 +8,15 @@ from ._lib import (  # noqa: F401
     ATTN_BF16,
     ATTN_F32,
     AttnError,
+    attn_cascade_decode,
+    attn_cascade_workspace_size,
     attn_decode_max_splits,
     attn_decode_paged,
     attn_decode_paged_noalloc,
     attn_decode_workspace_size,
     attn_device_error,
     attn_fwd,
+    attn_fwd_cross,
     attn_status_string,
     library_path,
     load_library,

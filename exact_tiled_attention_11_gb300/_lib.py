@@ -49,6 +49,13 @@ def load_library() -> ctypes.CDLL:
         vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.attn_fwd.restype = i32
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp]
+        lib.attn_fwd_cross.restype = i32
+        lib.attn_fwd_cross.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp]
+        lib.attn_cascade_workspace_size.restype = sz
+        lib.attn_cascade_workspace_size.argtypes = [i32, i32, i32, i32]
+        lib.attn_cascade_decode.restype = i32
+        lib.attn_cascade_decode.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                            f32, i32, vp, sz, vp]
         lib.attn_decode_workspace_size.restype = sz
         lib.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32]
         lib.attn_decode_max_splits.restype = i32
@@ -125,6 +132,33 @@ def attn_fwd(q, k, v, o=None, lse=None, *, causal=False, scale=None, stream=None
     return o, lse
 
 
+def attn_fwd_cross(q, k, v, o=None, lse=None, *, causal=False, scale=None, stream=None):
+    """Attention of Nq query rows against Nk keys.  q [B, H, Nq, d]; k, v [B, Hkv, Nk, d];
+    causal masking is aligned to the last key (row i attends keys j <= i + Nk - Nq).
+
+    Returns (o [B, H, Nq, d] in q's dtype, lse [B, H, Nq] fp32)."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, 4)
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("attn_fwd_cross takes bf16 or fp32 tensors")
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if k.shape != (B, Hkv, Nk, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, Nk, d] matching q")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, Nq, dtype=torch.float32, device=q.device)
+    _need(o, "o", q.dtype, 4)
+    _need(lse, "lse", torch.float32, 3)
+    scale = (1.0 / d ** 0.5) if scale is None else float(scale)
+    dt = ATTN_BF16 if q.dtype == torch.bfloat16 else ATTN_F32
+    _check("attn_fwd_cross", lib.attn_fwd_cross(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Nq, Nk,
+                                                d, 1 if causal else 0, scale, dt, _stream(stream, q.device)))
+    return o, lse
+
+
 def attn_decode_workspace_size(B: int, H: int, d: int, max_splits: int) -> int:
     return int(load_library().attn_decode_workspace_size(B, H, d, max_splits))
 
@@ -161,6 +195,44 @@ def attn_decode_paged(q, k_pages, v_pages, page_table, kv_lens, o=None, lse=None
         _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens), _ptr(o), _ptr(lse),
         B, H, Hkv, d, ps, maxp, P, (1.0 / d ** 0.5) if scale is None else float(scale), int(num_splits),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream, q.device)))
+    return o, lse
+
+
+def attn_cascade_workspace_size(B: int, H: int, d: int, max_splits: int) -> int:
+    return int(load_library().attn_cascade_workspace_size(B, H, d, max_splits))
+
+
+def attn_cascade_decode(q, prefix_k, prefix_v, k_pages, v_pages, page_table, kv_lens, o=None, lse=None, *,
+                        scale=None, num_splits=0, workspace=None, stream=None):
+    """Decode for requests sharing one prefix: q [B, H, d] bf16; prefix_k, prefix_v
+    [Hkv, prefix_len, d] bf16; each request's own suffix as in attn_decode_paged
+    (kv_lens counts suffix tokens).  Returns (o [B, H, d] bf16, lse [B, H] fp32)."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 3)
+    _need(prefix_k, "prefix_k", torch.bfloat16, 3)
+    _need(prefix_v, "prefix_v", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(kv_lens, "kv_lens", torch.int32, 1)
+    B, H, d = q.shape
+    P, Hkv, ps, _ = k_pages.shape
+    Lp = prefix_k.shape[1]
+    if prefix_k.shape != (Hkv, Lp, d) or prefix_v.shape != prefix_k.shape:
+        raise ValueError("prefix_k and prefix_v must be [Hkv, prefix_len, d]")
+    maxp = page_table.shape[1]
+    if o is None:
+        o = torch.empty(B, H, d, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, H, dtype=torch.float32, device=q.device)
+    S = num_splits if num_splits > 0 else lib.attn_decode_max_splits(B, H, Hkv, max(maxp, 1))
+    if workspace is None:
+        workspace = torch.empty(max(lib.attn_cascade_workspace_size(B, H, d, max(S, 1)), 256), dtype=torch.uint8,
+                                device=q.device)
+    _check("attn_cascade_decode", lib.attn_cascade_decode(
+        _ptr(q), _ptr(prefix_k), _ptr(prefix_v), Lp, _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens),
+        _ptr(o), _ptr(lse), B, H, Hkv, d, ps, maxp, P, (1.0 / d ** 0.5) if scale is None else float(scale),
+        int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream, q.device)))
     return o, lse
 
 

@@ -13,6 +13,7 @@
 namespace {
 
 using attn::PrefillMaps;
+using attn::PrefillOut;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -30,13 +31,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D bf16 tensor [d2][d1][d0] (d0 contiguous) with a box of (64, box1, 1) and 128-byte swizzle.
-bool make_map_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box1) {
+// 3-D bf16 tensor [d2][d1][d0] (d0 contiguous, nested strides) with a box of
+// (64, box1, box2) and 128-byte swizzle.
+bool make_map_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box1,
+                 uint32_t box2 = 1) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t dims[3] = {d0, d1, d2};
-  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
-  cuuint32_t box[3] = {64, box1, 1};
+  cuuint64_t dims[3] = {d0, std::max<uint64_t>(d1, 1), std::max<uint64_t>(d2, 1)};
+  cuuint64_t strides[2] = {d0 * 2, d0 * dims[1] * 2};
+  cuuint32_t box[3] = {64, box1, box2};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -68,6 +71,115 @@ int auto_splits(int B, int Hkv, int max_pages, int num_sms) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+size_t decode_ws_bytes(int B, int H, int d, int splits) {
+  const size_t n = static_cast<size_t>(B) * H * splits;
+  return 2 * align256(n * sizeof(float)) + align256(n * d * sizeof(float));
+}
+
+// ---------------------------------------------------------------------------
+// prefill over Nq query rows and Nk keys (Nq == Nk for attn_fwd)
+// ---------------------------------------------------------------------------
+attn_status_t fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Hkv,
+                       int Nq, int Nk, int d, int causal, float scale, attn_dtype_t dtype, attn_stream_t stream) {
+  if (B < 0 || H < 0 || Hkv < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || H == 0 || Nq == 0) return ATTN_OK;
+  if (Hkv == 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (q == nullptr || o == nullptr || (Nk > 0 && (k == nullptr || v == nullptr))) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
+    return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  PrefillOut out;
+  out.o = o;
+  out.lse = lse;
+  out.o_b = static_cast<long long>(H) * Nq * d;
+  out.o_h = static_cast<long long>(Nq) * d;
+  out.o_r = d;
+  out.l_b = static_cast<long long>(H) * Nq;
+  out.l_h = Nq;
+  out.l_r = 1;
+  cudaError_t e;
+  if (dtype == ATTN_F32) {
+    e = attn::launch_prefill_f32(static_cast<const float *>(q), static_cast<const float *>(k),
+                                 static_cast<const float *>(v), out, B, H, Hkv, Nq, Nk, d, causal != 0, scale, st);
+  } else {
+    // with Nk == 0 the K/V maps are never read; they only need a valid shape
+    const void *kb = Nk > 0 ? k : q;
+    const void *vb = Nk > 0 ? v : q;
+    PrefillMaps maps;
+    if (!make_map_3d(&maps.q, q, d, Nq, static_cast<uint64_t>(B) * H, 128) ||
+        !make_map_3d(&maps.k, kb, d, Nk, static_cast<uint64_t>(B) * Hkv, 128) ||
+        !make_map_3d(&maps.v, vb, d, Nk, static_cast<uint64_t>(B) * Hkv, 128))
+      return ATTN_ERR_CUDA;
+    e = attn::launch_prefill_bf16(maps, out, B, H, Hkv, Nq, Nk, d, causal != 0, scale, st);
+  }
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// paged split-KV decode; optional extra partial (O, LSE) per (sequence, head)
+// ---------------------------------------------------------------------------
+struct DecodePlan {
+  int splits;      // partial slots per (sequence, head)
+  int chunk;       // pages per chunk
+  bool has_pages;  // anything to stream at all
+};
+
+attn_status_t decode_check(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,
+                           const int32_t *kv_lens, const void *o, const float *lse, int B, int H, int Hkv, int d,
+                           int page_size, int max_pages_per_seq, int num_pages, float scale, const void *workspace) {
+  if (B < 0 || H < 0 || Hkv < 0 || max_pages_per_seq < 0 || num_pages < 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || H == 0) return ATTN_OK;
+  if (Hkv == 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (q == nullptr || o == nullptr || kv_lens == nullptr || workspace == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || (lse && !aligned16(lse)) || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
+  if (d != 128 || page_size != 16 || H / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
+  if (max_pages_per_seq > 0 && num_pages > 0) {
+    if (k_pages == nullptr || v_pages == nullptr || page_table == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(k_pages) || !aligned16(v_pages)) return ATTN_ERR_INVALID_ARG;
+  }
+  return ATTN_OK;
+}
+
+DecodePlan decode_plan(int B, int Hkv, int max_pages_per_seq, int num_pages, int num_splits) {
+  const int mp = std::max(max_pages_per_seq, 1);
+  const int S = num_splits > 0 ? std::min(num_splits, mp) : auto_splits(B, Hkv, mp, device_sm_count());
+  const int chunk = ceil_div(mp, S);
+  DecodePlan p;
+  p.splits = ceil_div(mp, chunk);  // partial slots any sequence can need
+  p.chunk = chunk;
+  p.has_pages = max_pages_per_seq > 0 && num_pages > 0;
+  return p;
+}
+
+attn_status_t decode_launch(const DecodePlan &plan, const void *q, const void *k_pages, const void *v_pages,
+                            const int32_t *page_table, const int32_t *kv_lens, void *o, float *lse, int B, int H,
+                            int Hkv, int d, int page_size, int max_pages_per_seq, int num_pages, float scale,
+                            void *workspace, const void *extra_o, const float *extra_lse, cudaStream_t st) {
+  const size_t n = static_cast<size_t>(B) * H * plan.splits;
+  float *ws_m = static_cast<float *>(workspace);
+  float *ws_l = reinterpret_cast<float *>(static_cast<char *>(workspace) + align256(n * sizeof(float)));
+  float *ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + 2 * align256(n * sizeof(float)));
+  if (plan.has_pages) {
+    CUtensorMap tm_k, tm_v;
+    const uint64_t rows = static_cast<uint64_t>(num_pages) * Hkv;
+    if (!make_map_3d(&tm_k, k_pages, d, page_size, rows, page_size) ||
+        !make_map_3d(&tm_v, v_pages, d, page_size, rows, page_size))
+      return ATTN_ERR_CUDA;
+    cudaError_t e = attn::launch_decode_split(tm_k, tm_v, q, page_table, kv_lens, ws_m, ws_l, ws_o, B, H, Hkv,
+                                              max_pages_per_seq, num_pages, plan.chunk, plan.splits, scale, st);
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  // with no pages at all every sequence's own keys are empty: only the extra partial (if any) counts
+  cudaError_t e = attn::launch_merge(ws_m, ws_l, ws_o, nullptr, kv_lens, page_size,
+                                     plan.has_pages ? plan.chunk : 1 << 30, B, H, plan.splits, d, o, true, lse,
+                                     extra_o, extra_lse, st);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -86,36 +198,17 @@ const char *attn_status_string(attn_status_t s) {
 
 attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Hkv, int N,
                        int d, int causal, float scale, attn_dtype_t dtype, attn_stream_t stream) {
-  if (B < 0 || H < 0 || Hkv < 0 || N < 0) return ATTN_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !(scale < INFINITY)) return ATTN_ERR_INVALID_ARG;
-  if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
-  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
-  if (Hkv == 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
-    return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (dtype == ATTN_F32) {
-    e = attn::launch_prefill_f32(static_cast<const float *>(q), static_cast<const float *>(k),
-                                 static_cast<const float *>(v), static_cast<float *>(o), lse, B, H, Hkv, N, d,
-                                 causal != 0, scale, st);
-  } else {
-    PrefillMaps maps;
-    if (!make_map_3d(&maps.q, q, d, N, static_cast<uint64_t>(B) * H, 128) ||
-        !make_map_3d(&maps.k, k, d, N, static_cast<uint64_t>(B) * Hkv, 128) ||
-        !make_map_3d(&maps.v, v, d, N, static_cast<uint64_t>(B) * Hkv, 128))
-      return ATTN_ERR_CUDA;
-    e = attn::launch_prefill_bf16(maps, o, lse, B, H, Hkv, N, d, causal != 0, scale, 0, st);
-  }
-  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return fwd_impl(q, k, v, o, lse, B, H, Hkv, N, N, d, causal, scale, dtype, stream);
+}
+
+attn_status_t attn_fwd_cross(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Hkv,
+                             int Nq, int Nk, int d, int causal, float scale, attn_dtype_t dtype, attn_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, causal, scale, dtype, stream);
 }
 
 size_t attn_decode_workspace_size(int B, int H, int d, int max_splits) {
   if (B <= 0 || H <= 0 || d <= 0 || max_splits <= 0) return 0;
-  const size_t n = static_cast<size_t>(B) * H * max_splits;
-  return 2 * align256(n * sizeof(float)) + align256(n * d * sizeof(float));
+  return decode_ws_bytes(B, H, d, max_splits);
 }
 
 int attn_decode_max_splits(int B, int H, int Hkv, int max_pages_per_seq) {
@@ -127,45 +220,69 @@ attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *
                                 const int32_t *kv_lens, void *o, float *lse, int B, int H, int Hkv, int d,
                                 int page_size, int max_pages_per_seq, int num_pages, float scale, int num_splits,
                                 void *workspace, size_t workspace_bytes, attn_stream_t stream) {
-  if (B < 0 || H < 0 || Hkv < 0 || max_pages_per_seq < 0 || num_pages < 0) return ATTN_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !(scale < INFINITY)) return ATTN_ERR_INVALID_ARG;
-  if (B == 0 || H == 0) return ATTN_OK;
-  if (Hkv == 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (q == nullptr || o == nullptr || kv_lens == nullptr || workspace == nullptr) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(o) || (lse && !aligned16(lse)) || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
-  if (d != 128 || page_size != 16 || H / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
-  if (max_pages_per_seq > 0 && num_pages > 0) {
-    if (k_pages == nullptr || v_pages == nullptr || page_table == nullptr) return ATTN_ERR_INVALID_ARG;
-    if (!aligned16(k_pages) || !aligned16(v_pages)) return ATTN_ERR_INVALID_ARG;
-  }
-  const int mp = std::max(max_pages_per_seq, 1);
-  const int S = num_splits > 0 ? std::min(num_splits, mp) : auto_splits(B, Hkv, mp, device_sm_count());
-  const int chunk = ceil_div(mp, S);
-  const int S_used = ceil_div(mp, chunk);  // partial slots any sequence can need
-  if (workspace_bytes < attn_decode_workspace_size(B, H, d, S_used)) return ATTN_ERR_WORKSPACE;
-  if (S_used > 65535 || B > 65535) return ATTN_ERR_UNSUPPORTED;
+  attn_status_t s = decode_check(q, k_pages, v_pages, page_table, kv_lens, o, lse, B, H, Hkv, d, page_size,
+                                 max_pages_per_seq, num_pages, scale, workspace);
+  if (s != ATTN_OK || B == 0 || H == 0) return s;
+  const DecodePlan plan = decode_plan(B, Hkv, max_pages_per_seq, num_pages, num_splits);
+  if (workspace_bytes < decode_ws_bytes(B, H, d, plan.splits)) return ATTN_ERR_WORKSPACE;
+  if (plan.splits > 65535 || B > 65535) return ATTN_ERR_UNSUPPORTED;
+  return decode_launch(plan, q, k_pages, v_pages, page_table, kv_lens, o, lse, B, H, Hkv, d, page_size,
+                       max_pages_per_seq, num_pages, scale, workspace, nullptr, nullptr,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
 
-  const size_t n = static_cast<size_t>(B) * H * S_used;
-  float *ws_m = static_cast<float *>(workspace);
-  float *ws_l = reinterpret_cast<float *>(static_cast<char *>(workspace) + align256(n * sizeof(float)));
-  float *ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + 2 * align256(n * sizeof(float)));
+size_t attn_cascade_workspace_size(int B, int H, int d, int max_splits) {
+  if (B <= 0 || H <= 0 || d <= 0 || max_splits <= 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * H;
+  return decode_ws_bytes(B, H, d, max_splits) + align256(rows * d * 2) + align256(rows * sizeof(float));
+}
+
+attn_status_t attn_cascade_decode(const void *q, const void *prefix_k, const void *prefix_v, int prefix_len,
+                                  const void *k_pages, const void *v_pages, const int32_t *page_table,
+                                  const int32_t *kv_lens, void *o, float *lse, int B, int H, int Hkv, int d,
+                                  int page_size, int max_pages_per_seq, int num_pages, float scale, int num_splits,
+                                  void *workspace, size_t workspace_bytes, attn_stream_t stream) {
+  if (prefix_len < 0) return ATTN_ERR_INVALID_ARG;
+  attn_status_t s = decode_check(q, k_pages, v_pages, page_table, kv_lens, o, lse, B, H, Hkv, d, page_size,
+                                 max_pages_per_seq, num_pages, scale, workspace);
+  if (s != ATTN_OK || B == 0 || H == 0) return s;
+  if (prefix_len > 0) {
+    if (prefix_k == nullptr || prefix_v == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(prefix_k) || !aligned16(prefix_v)) return ATTN_ERR_INVALID_ARG;
+  }
+  const DecodePlan plan = decode_plan(B, Hkv, max_pages_per_seq, num_pages, num_splits);
+  if (workspace_bytes < attn_cascade_workspace_size(B, H, d, plan.splits)) return ATTN_ERR_WORKSPACE;
+  if (plan.splits > 65535 || B > 65535) return ATTN_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-  if (max_pages_per_seq > 0 && num_pages > 0) {
-    CUtensorMap tm_k, tm_v;
-    const uint64_t rows = static_cast<uint64_t>(num_pages) * Hkv;
-    if (!make_map_3d(&tm_k, k_pages, d, page_size, rows, page_size) ||
-        !make_map_3d(&tm_v, v_pages, d, page_size, rows, page_size))
+  const size_t rows = static_cast<size_t>(B) * H;
+  char *prefix_area = static_cast<char *>(workspace) + decode_ws_bytes(B, H, d, plan.splits);
+  void *o_prefix = prefix_area;                                                         // [B, H, d] bf16
+  float *lse_prefix = reinterpret_cast<float *>(prefix_area + align256(rows * d * 2));  // [B, H] fp32
+  if (prefix_len > 0) {
+    // The shared prefix once for every request: one attention whose query rows
+    // are the B requests' tokens (per head), against the prefix keys.
+    PrefillMaps maps;
+    maps.q_rows_outer = true;  // q [B, H, d] seen as (d, H, B): the rows (requests) are the outer dimension
+    if (!make_map_3d(&maps.q, q, d, H, B, 1, 128) || !make_map_3d(&maps.k, prefix_k, d, prefix_len, Hkv, 128) ||
+        !make_map_3d(&maps.v, prefix_v, d, prefix_len, Hkv, 128))
       return ATTN_ERR_CUDA;
-    cudaError_t e = attn::launch_decode_split(tm_k, tm_v, q, page_table, kv_lens, ws_m, ws_l, ws_o, B, H, Hkv,
-                                              max_pages_per_seq, num_pages, chunk, S_used, scale, st);
-    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+    PrefillOut out;
+    out.o = o_prefix;
+    out.lse = lse_prefix;
+    out.o_b = 0;
+    out.o_h = d;
+    out.o_r = static_cast<long long>(H) * d;
+    out.l_b = 0;
+    out.l_h = 1;
+    out.l_r = H;
+    if (attn::launch_prefill_bf16(maps, out, 1, H, Hkv, B, prefix_len, d, false, scale, st) != cudaSuccess)
+      return ATTN_ERR_CUDA;
   }
-  // with no pages at all every sequence is empty: the merge writes O = 0, LSE = -inf
-  cudaError_t e = attn::launch_merge(ws_m, ws_l, ws_o, nullptr, kv_lens, page_size,
-                                     (max_pages_per_seq > 0 && num_pages > 0) ? chunk : 1 << 30, B, H, S_used, d, o,
-                                     true, lse, st);
-  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  // each request's own suffix, merged with the prefix result as one more partial
+  return decode_launch(plan, q, k_pages, v_pages, page_table, kv_lens, o, lse, B, H, Hkv, d, page_size,
+                       max_pages_per_seq, num_pages, scale, workspace, prefix_len > 0 ? o_prefix : nullptr,
+                       prefix_len > 0 ? lse_prefix : nullptr, st);
 }
 
 attn_status_t merge_partials(const float *m, const float *l, const float *o_tilde, const int32_t *num_parts, int B,
@@ -177,7 +294,7 @@ attn_status_t merge_partials(const float *m, const float *l, const float *o_tild
   if (!aligned16(o_tilde) || !aligned16(o) || (lse && !aligned16(lse))) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   cudaError_t e = attn::launch_merge(m, l, o_tilde, num_parts, nullptr, 0, 1, B, H, S, d, o, o_dtype == ATTN_BF16,
-                                     lse, reinterpret_cast<cudaStream_t>(stream));
+                                     lse, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

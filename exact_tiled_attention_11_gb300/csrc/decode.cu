@@ -358,11 +358,15 @@ __global__ void __launch_bounds__(kThreads)
 // o~ = sum exp(m_s - m) o~_s, O = o~ / l, LSE = m + ln l.
 // The partial count is num_parts[b], S when num_parts is null, or -- for the
 // decode path -- derived from kv_lens as ceil(ceil(L / page) / chunk).
+// An optional extra partial per (sequence, head) comes as a normalised output
+// with its log-sum-exp: (m, l, o~) = (LSE, 1, O) -- e.g. the shared-prefix
+// part of cascade attention.
 template <int D, typename OutT>
 __global__ void __launch_bounds__(256)
     merge_kernel(const float *__restrict__ m_in, const float *__restrict__ l_in, const float *__restrict__ o_in,
                  const int32_t *__restrict__ num_parts, const int32_t *__restrict__ kv_lens, int page_size,
-                 int chunk_pages, int B, int H, int S, OutT *__restrict__ o_out, float *__restrict__ lse_out) {
+                 int chunk_pages, int B, int H, int S, OutT *__restrict__ o_out, float *__restrict__ lse_out,
+                 const __nv_bfloat16 *__restrict__ extra_o, const float *__restrict__ extra_lse) {
   constexpr int E = D / 32;  // elements per lane
   const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -380,6 +384,8 @@ __global__ void __launch_bounds__(256)
 
   float m = -INFINITY;
   for (int s = lane; s < n; s += 32) m = fmaxf(m, m_in[base + s]);
+  const float m_extra = extra_lse != nullptr ? extra_lse[warp_global] : -INFINITY;
+  m = fmaxf(m, m_extra);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
 
@@ -418,6 +424,13 @@ __global__ void __launch_bounds__(256)
         for (int j = 0; j < E; ++j) o[j] += w[u] * ov[u][j];
       }
     }
+  }
+  if (m != -INFINITY && m_extra != -INFINITY) {
+    const float w = expf(m_extra - m);
+    l += w;
+    const __nv_bfloat16 *src = extra_o + static_cast<size_t>(warp_global) * D + lane * E;
+#pragma unroll
+    for (int j = 0; j < E; ++j) o[j] += w * __bfloat162float(src[j]);
   }
   const float inv = (l > 0.f) ? 1.f / l : 0.f;
   OutT *dst = o_out + static_cast<size_t>(warp_global) * D + lane * E;
@@ -466,14 +479,16 @@ cudaError_t launch_decode_split(const CUtensorMap &tm_k, const CUtensorMap &tm_v
 
 cudaError_t launch_merge(const float *m, const float *l, const float *o_tilde, const int32_t *num_parts,
                          const int32_t *kv_lens, int page_size, int chunk_pages, int B, int H, int S, int d, void *o,
-                         bool out_bf16, float *lse, cudaStream_t stream) {
+                         bool out_bf16, float *lse, const void *extra_o, const float *extra_lse,
+                         cudaStream_t stream) {
   const int warps = B * H;
   const int threads = 256;
   const int blocks = (warps * 32 + threads - 1) / threads;
   if (blocks == 0) return cudaSuccess;
 #define ATTN_MERGE_LAUNCH(DD, T)                                                                              \
   merge_kernel<DD, T><<<blocks, threads, 0, stream>>>(m, l, o_tilde, num_parts, kv_lens, page_size, chunk_pages, \
-                                                      B, H, S, static_cast<T *>(o), lse)
+                                                      B, H, S, static_cast<T *>(o), lse,                          \
+                                                      static_cast<const __nv_bfloat16 *>(extra_o), extra_lse)
   if (d == 128) {
     if (out_bf16) ATTN_MERGE_LAUNCH(128, __nv_bfloat16);
     else ATTN_MERGE_LAUNCH(128, float);

@@ -14,20 +14,35 @@ cudaError_t launch_decode_split(const CUtensorMap &tm_k, const CUtensorMap &tm_v
                                 const int32_t *page_table, const int32_t *kv_lens, float *ws_m, float *ws_l,
                                 float *ws_o, int B, int H, int Hkv, int max_pages, int num_pages, int chunk_pages,
                                 int S, float scale, cudaStream_t stream);
+// extra_o / extra_lse (nullable): one more partial per (sequence, head), given as a
+// normalised output O [B, H, d] bf16 with its LSE [B, H], i.e. (m, l, o~) = (LSE, 1, O).
 cudaError_t launch_merge(const float *m, const float *l, const float *o_tilde, const int32_t *num_parts,
                          const int32_t *kv_lens, int page_size, int chunk_pages, int B, int H, int S, int d, void *o,
-                         bool out_bf16, float *lse, cudaStream_t stream);
+                         bool out_bf16, float *lse, const void *extra_o, const float *extra_lse,
+                         cudaStream_t stream);
 
-// prefill_f32.cu
-cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, float *o, float *lse, int B, int H,
-                               int Hkv, int N, int d, bool causal, float scale, cudaStream_t stream);
+// Where the prefill kernels write O and the LSE: element strides of the batch,
+// head and query-row dimensions (d is contiguous).  The plain [B, H, Nq, d] /
+// [B, H, Nq] layout is {H*Nq*d, Nq*d, d} / {H*Nq, Nq, 1}.
+struct PrefillOut {
+  void *o;
+  float *lse;  // may be null
+  long long o_b, o_h, o_r;
+  long long l_b, l_h, l_r;
+};
 
-// prefill_bf16.cu
+// prefill_f32.cu (q [B, H, Nq, d], k/v [B, Hkv, Nk, d])
+cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const PrefillOut &out, int B, int H,
+                               int Hkv, int Nq, int Nk, int d, bool causal, float scale, cudaStream_t stream);
+
+// prefill_bf16.cu: Q, K, V through TMA maps whose dimensions are (d, rows, B * heads);
+// with q_rows_outer the Q map is (d, B * H, rows) instead (box (64, 1, 128)).
 struct PrefillMaps {
   CUtensorMap q, k, v;
+  bool q_rows_outer = false;
 };
-cudaError_t launch_prefill_bf16(const PrefillMaps &maps, void *o, float *lse, int B, int H, int Hkv, int N, int d,
-                                bool causal, float scale, int num_sms, cudaStream_t stream);
+cudaError_t launch_prefill_bf16(const PrefillMaps &maps, const PrefillOut &out, int B, int H, int Hkv, int Nq,
+                                int Nk, int d, bool causal, float scale, cudaStream_t stream);
 
 // Per-translation-unit device error words (see common.cuh).
 cudaError_t device_error_decode(unsigned int *value, bool clear);

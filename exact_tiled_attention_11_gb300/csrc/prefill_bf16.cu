@@ -11,6 +11,9 @@
 // GB300 mapping: one CTA per PAIR of 128-row query tiles (A and B) of one
 // (batch, head), 384 threads, one CTA per SM.  Each tile is a chain
 //     S_c(j) = Q_c K_j^T -> softmax_c(j) -> P_c(j) -> O_c += P_c(j) V_j
+// over Nq query rows and Nk keys; with causal masking query row i attends
+// keys j <= i + (Nk - Nq), i.e. the mask is aligned to the last key (for
+// self-attention, Nq = Nk, this is j <= i).
 // and, because P lives in shared memory rather than over S, S_c(j+1) can be
 // computed as soon as softmax has loaded S_c(j) into registers: the tensor
 // core works on the next score tile (and on the other chain) while the
@@ -150,8 +153,8 @@ __device__ __forceinline__ void rescale_o_chunk(uint32_t taddr, float corr) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ o,
-                        float *__restrict__ lse, int B, int H, int Hkv, int N, int causal, float scale_log2) {
+                        const __grid_constant__ CUtensorMap tm_v, const PrefillOut out, int B, int H, int Hkv,
+                        int Nq, int Nk, int causal, float scale_log2, int q_rows_outer) {
   using Smem = PrefillSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -160,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   // ---- which (query-tile pair, batch, head): heaviest causal pairs first
-  const int n_pairs = (N + 2 * BM - 1) / (2 * BM);
+  const int n_pairs = (Nq + 2 * BM - 1) / (2 * BM);
   const int bh_count = B * H;
   const int rank = blockIdx.x / bh_count;
   const int bh = blockIdx.x % bh_count;
@@ -169,10 +172,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = bh % H;
   const int kvh = h / (H / Hkv);
   const int row0[2] = {2 * t * BM, (2 * t + 1) * BM};
-  const bool has_b = row0[1] < N;
-  const int n_kt_all = (N + BN - 1) / BN;
-  // key tiles each chain visits: causal tile i attends tiles 0..i
-  const int n_tiles[2] = {causal ? 2 * t + 1 : n_kt_all, has_b ? (causal ? 2 * t + 2 : n_kt_all) : 0};
+  const bool has_b = row0[1] < Nq;
+  const int n_kt_all = (Nk + BN - 1) / BN;
+  const int shift = Nk - Nq;
+  // key tiles each chain visits: causal, up to the tile of its last row's last key
+  auto tiles_of = [&](int r0) {
+    if (!causal) return n_kt_all;
+    const int last_key = min(r0 + BM, Nq) - 1 + shift;
+    return last_key < 0 ? 0 : min(n_kt_all, last_key / BN + 1);
+  };
+  const int n_tiles[2] = {tiles_of(row0[0]), has_b ? tiles_of(row0[1]) : 0};
   const int n_kv = max(n_tiles[0], n_tiles[1]);
 
   if (threadIdx.x == 0) {
@@ -219,7 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < (has_b ? 2 : 1); ++c)
 #pragma unroll
         for (int x = 0; x < D / 64; ++x)
-          tma_load_3d_hint(smem_u32(sm.q[c]) + x * kBoxBytes, &tm_q, qbar, x * 64, row0[c], b * H + h, once);
+          // Q map dimensions: (d, rows, B * H), or (d, B * H, rows) when the query rows are the outer dimension
+          tma_load_3d_hint(smem_u32(sm.q[c]) + x * kBoxBytes, &tm_q, qbar, x * 64, q_rows_outer ? b * H + h : row0[c],
+                           q_rows_outer ? row0[c] : b * H + h, once);
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int ks = j % kKStages;
@@ -362,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_addr = tmem + lane_addr + c * BN;
     const uint32_t o_addr = tmem + lane_addr + 2 * BN + c * BN;
     const uint32_t p_row = smem_u32(sm.p[c]) + row * 128;  // this row in each 64-key swizzled box
-    const int lim = causal ? min(q_row + 1, N) : N;        // keys [0, lim) are attended by this row
+    const int lim = causal ? min(q_row + shift + 1, Nk) : Nk;  // keys [0, lim) are attended by this row
     const uint64_t scale2 = f2(scale_log2, scale_log2);
     float m_ref = -INFINITY;  // reference maximum (log2 units) that p and o~ are relative to
     float l = 0.f;
@@ -404,11 +415,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // move the reference only when the row maximum outgrows it by more than 2^8
       const bool move = m_new > m_ref + kRescaleThreshold;
       const float m_next = move ? m_new : m_ref;
-      const float corr = ex2_approx(m_ref - m_next);  // 1 when kept; 0 on the first tile
+      // 1 when kept (also while the row has met no key at all); 0 on the row's first key
+      const float corr = (m_next == m_ref) ? 1.f : ex2_approx(m_ref - m_next);
       m_ref = m_next;
 
       // p = 2^(s * scale * log2(e) - m_ref), summed in eight partial sums, packed to bf16
-      const uint64_t negm2 = f2(-m_ref, -m_ref);
+      // (a row that has met no key yet has every s = -inf and takes reference 0: p = 0)
+      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      const uint64_t negm2 = f2(neg_m, neg_m);
       uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pr[2][32];
 #pragma unroll
@@ -460,8 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc05::fence_after_sync();
         const float inv = (l > 0.f) ? 1.f / l : 0.f;
         const uint64_t inv2 = f2(inv, inv);
-        const bool store = q_row < N;
-        __nv_bfloat16 *orow = o + ((static_cast<size_t>(b) * H + h) * N + (store ? q_row : 0)) * D;
+        const bool store = q_row < Nq;
+        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(out.o) + b * out.o_b + h * out.o_h +
+                              static_cast<long long>(store ? q_row : 0) * out.o_r;
 #pragma unroll
         for (int q4 = 0; q4 < D / 32; ++q4) {
           uint32_t orr[32];
@@ -481,9 +496,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
           }
         }
-        if (store && lse != nullptr)
-          lse[(static_cast<size_t>(b) * H + h) * N + q_row] = (l > 0.f) ? m_ref * kLn2 + logf(l) : -INFINITY;
+        if (store && out.lse != nullptr)
+          out.lse[b * out.l_b + h * out.l_h + static_cast<long long>(q_row) * out.l_r] =
+              (l > 0.f) ? m_ref * kLn2 + logf(l) : -INFINITY;
       }
+    } else if (n_c == 0 && q_row < Nq) {
+      // a tile whose rows attend no key (causal, Nq > Nk): O = 0, LSE = -inf
+      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(out.o) + b * out.o_b + h * out.o_h +
+                                             static_cast<long long>(q_row) * out.o_r);
+#pragma unroll
+      for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
+      if (out.lse != nullptr) out.lse[b * out.l_b + h * out.l_h + static_cast<long long>(q_row) * out.l_r] = -INFINITY;
     }
   }
 
@@ -496,19 +519,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D>
-cudaError_t launch_d(const PrefillMaps &maps, void *o, float *lse, int B, int H, int Hkv, int N, bool causal,
-                     float scale, cudaStream_t stream) {
+cudaError_t launch_d(const PrefillMaps &maps, const PrefillOut &out, int B, int H, int Hkv, int Nq, int Nk,
+                     bool causal, float scale, cudaStream_t stream) {
   // One CTA per SM: the kernel holds all 512 tensor-memory columns.
   const size_t smem = std::max<size_t>(sizeof(PrefillSmem<D>) + 1024, 120 * 1024);
   auto kern = prefill_bf16_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const long long n_pairs = (N + 2 * BM - 1) / (2 * BM);
+  const long long n_pairs = (Nq + 2 * BM - 1) / (2 * BM);
   const long long blocks = n_pairs * B * H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(maps.q, maps.k, maps.v,
-                                                                   static_cast<__nv_bfloat16 *>(o), lse, B, H, Hkv, N,
-                                                                   causal ? 1 : 0, scale * kLog2e);
+  kern<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(maps.q, maps.k, maps.v, out, B, H, Hkv, Nq, Nk,
+                                                                   causal ? 1 : 0, scale * kLog2e,
+                                                                   maps.q_rows_outer ? 1 : 0);
   return cudaGetLastError();
 }
 
@@ -516,10 +539,10 @@ cudaError_t launch_d(const PrefillMaps &maps, void *o, float *lse, int B, int H,
 
 ATTN_DEFINE_ERROR_ACCESSOR(device_error_prefill_bf16)
 
-cudaError_t launch_prefill_bf16(const PrefillMaps &maps, void *o, float *lse, int B, int H, int Hkv, int N, int d,
-                                bool causal, float scale, int /*num_sms*/, cudaStream_t stream) {
-  if (d == 64) return launch_d<64>(maps, o, lse, B, H, Hkv, N, causal, scale, stream);
-  return launch_d<128>(maps, o, lse, B, H, Hkv, N, causal, scale, stream);
+cudaError_t launch_prefill_bf16(const PrefillMaps &maps, const PrefillOut &out, int B, int H, int Hkv, int Nq,
+                                int Nk, int d, bool causal, float scale, cudaStream_t stream) {
+  if (d == 64) return launch_d<64>(maps, out, B, H, Hkv, Nq, Nk, causal, scale, stream);
+  return launch_d<128>(maps, out, B, H, Hkv, Nq, Nk, causal, scale, stream);
 }
 
 }  // namespace attn

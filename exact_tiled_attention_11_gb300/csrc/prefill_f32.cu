@@ -26,8 +26,7 @@ constexpr int kTile = 32;       // keys per tile (one per lane)
 template <int D>
 __global__ void __launch_bounds__(kRowsPerCta * 32)
     prefill_f32_kernel(const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
-                       float *__restrict__ o, float *__restrict__ lse, int H, int Hkv, int N, int causal,
-                       float scale) {
+                       PrefillOut out, int H, int Hkv, int Nq, int Nk, int causal, float scale) {
   constexpr int E = D / 32;
   __shared__ float ks[kTile][D + 1];  // +1: lane j reads row j without bank conflicts
   __shared__ float vs[kTile][D];
@@ -40,11 +39,12 @@ __global__ void __launch_bounds__(kRowsPerCta * 32)
   const int lane = threadIdx.x & 31;
   const int row0 = blockIdx.x * kRowsPerCta;
   const int row = row0 + warp;
-  const bool live_row = row < N;
+  const bool live_row = row < Nq;
 
-  const float *qh = q + (static_cast<size_t>(b) * H + h) * N * D;
-  const float *kh = k + (static_cast<size_t>(b) * Hkv + kvh) * N * D;
-  const float *vh = v + (static_cast<size_t>(b) * Hkv + kvh) * N * D;
+  const float *qh = q + (static_cast<size_t>(b) * H + h) * Nq * D;
+  const float *kh = k + (static_cast<size_t>(b) * Hkv + kvh) * Nk * D;
+  const float *vh = v + (static_cast<size_t>(b) * Hkv + kvh) * Nk * D;
+  const int shift = Nk - Nq;  // causal: query row i attends keys j <= i + shift (aligned to the last key)
 
   for (int e = lane; e < D; e += 32) qs[warp][e] = live_row ? qh[static_cast<size_t>(row) * D + e] : 0.f;
 
@@ -53,20 +53,21 @@ __global__ void __launch_bounds__(kRowsPerCta * 32)
 #pragma unroll
   for (int j = 0; j < E; ++j) acc[j] = 0.0;
 
-  const int last_row = min(N, row0 + kRowsPerCta) - 1;
-  const int key_end = causal ? last_row + 1 : N;  // tiles wholly after the CTA's last row are skipped
+  const int last_row = min(Nq, row0 + kRowsPerCta) - 1;
+  // tiles wholly after the CTA's last row are skipped
+  const int key_end = causal ? max(0, min(Nk, last_row + shift + 1)) : Nk;
   for (int t0 = 0; t0 < key_end; t0 += kTile) {
     __syncthreads();
     for (int idx = threadIdx.x; idx < kTile * D; idx += kRowsPerCta * 32) {
       const int r = idx / D, e = idx % D;
-      const bool in = t0 + r < N;
+      const bool in = t0 + r < Nk;
       ks[r][e] = in ? kh[static_cast<size_t>(t0 + r) * D + e] : 0.f;
       vs[r][e] = in ? vh[static_cast<size_t>(t0 + r) * D + e] : 0.f;
     }
     __syncthreads();
 
     const int key = t0 + lane;
-    const bool attend = live_row && key < N && (!causal || key <= row);
+    const bool attend = live_row && key < Nk && (!causal || key <= row + shift);
     double s = -INFINITY;
     if (attend) {
       double dot = 0.0;
@@ -97,12 +98,12 @@ __global__ void __launch_bounds__(kRowsPerCta * 32)
   }
 
   if (!live_row) return;
-  float *oh = o + ((static_cast<size_t>(b) * H + h) * N + row) * D;
+  float *oh = static_cast<float *>(out.o) + b * out.o_b + h * out.o_h + row * out.o_r;
   const double inv = (l > 0.0) ? 1.0 / l : 0.0;
 #pragma unroll
   for (int j = 0; j < E; ++j) oh[lane + 32 * j] = static_cast<float>(acc[j] * inv);
-  if (lse != nullptr && lane == 0) {
-    lse[(static_cast<size_t>(b) * H + h) * N + row] = (l > 0.0) ? static_cast<float>(m + log(l)) : -INFINITY;
+  if (out.lse != nullptr && lane == 0) {
+    out.lse[b * out.l_b + h * out.l_h + row * out.l_r] = (l > 0.0) ? static_cast<float>(m + log(l)) : -INFINITY;
   }
 }
 
@@ -110,13 +111,13 @@ __global__ void __launch_bounds__(kRowsPerCta * 32)
 
 ATTN_DEFINE_ERROR_ACCESSOR(device_error_prefill_f32)
 
-cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, float *o, float *lse, int B, int H,
-                               int Hkv, int N, int d, bool causal, float scale, cudaStream_t stream) {
-  dim3 grid((N + kRowsPerCta - 1) / kRowsPerCta, H, B);
+cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const PrefillOut &out, int B, int H,
+                               int Hkv, int Nq, int Nk, int d, bool causal, float scale, cudaStream_t stream) {
+  dim3 grid((Nq + kRowsPerCta - 1) / kRowsPerCta, H, B);
   if (d == 64) {
-    prefill_f32_kernel<64><<<grid, kRowsPerCta * 32, 0, stream>>>(q, k, v, o, lse, H, Hkv, N, causal ? 1 : 0, scale);
+    prefill_f32_kernel<64><<<grid, kRowsPerCta * 32, 0, stream>>>(q, k, v, out, H, Hkv, Nq, Nk, causal ? 1 : 0, scale);
   } else {
-    prefill_f32_kernel<128><<<grid, kRowsPerCta * 32, 0, stream>>>(q, k, v, o, lse, H, Hkv, N, causal ? 1 : 0, scale);
+    prefill_f32_kernel<128><<<grid, kRowsPerCta * 32, 0, stream>>>(q, k, v, out, H, Hkv, Nq, Nk, causal ? 1 : 0, scale);
   }
   return cudaGetLastError();
 }

@@ -79,6 +79,21 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
                        attn_dtype_t dtype, attn_stream_t stream);
 
 /*
+ * attn_fwd_cross -- attn_fwd with Nq query rows against Nk keys (Nq may differ
+ * from Nk: cross attention, or a chunk of new queries against a cache that
+ * ends with them).  With causal = 1 the mask is aligned to the last key:
+ * query row i attends key j iff j <= i + (Nk - Nq), the alignment of the
+ * naive causal attention in "3.4 Attention Kernels", "Code"; rows that attend
+ * no key get O = 0 and LSE = -inf.  Same algorithm and citations as attn_fwd.
+ *
+ *  q     [B, H, Nq, d]    k, v [B, Hkv, Nk, d]    o [B, H, Nq, d]    lse [B, H, Nq]
+ *  Nq, Nk >= 0; Nq == 0 (or B == 0, H == 0) is a no-op.
+ */
+attn_status_t attn_fwd_cross(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                             attn_dtype_t dtype, attn_stream_t stream);
+
+/*
  * attn_decode_workspace_size -- bytes of device workspace attn_decode_paged
  * needs for up to max_splits partial results per (sequence, query head):
  * fp32 m and l [B, H, max_splits] and fp32 o~ [B, H, max_splits, d], each
@@ -128,6 +143,43 @@ attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *
  * workspace).  Returns 0 for invalid arguments.
  */
 int attn_decode_max_splits(int B, int H, int Hkv, int max_pages_per_seq);
+
+/*
+ * attn_cascade_workspace_size -- bytes of device workspace attn_cascade_decode
+ * needs: the decode partials for max_splits chunks plus the shared-prefix
+ * result (bf16 O [B, H, d] and fp32 LSE [B, H]), each region 256-byte aligned.
+ * Returns 0 for invalid arguments.
+ */
+size_t attn_cascade_workspace_size(int B, int H, int d, int max_splits);
+
+/*
+ * attn_cascade_decode -- decode for B requests that share one prefix of
+ * prefix_len tokens and each have their own paged suffix (cascade attention).
+ *
+ * Follows "3.4 Attention Kernels", "Paged and ragged layouts: FlashInfer"
+ * (attention over the shared prefix is computed once for all requests' queries
+ * and merged with each request's own-suffix attention by the merge operator)
+ * and "Check your understanding" (attention over prefix U suffix is the
+ * log-sum-exp merge of the two).  The prefix pass is one attention whose query
+ * rows are the B requests' tokens (per head) against the prefix keys, on the
+ * tensor-core prefill kernel; the suffix pass is attn_decode_paged's split
+ * kernel; the merge kernel combines the suffix chunks' partials with the
+ * prefix result taken as the partial (m, l, o~) = (LSE_prefix, 1, O_prefix).
+ *
+ *  q                     [B, H, d]                  bf16   one query token per request
+ *  prefix_k, prefix_v    [Hkv, prefix_len, d]       bf16   the shared prefix's keys/values
+ *  k_pages ... kv_lens   the requests' own suffixes, exactly as attn_decode_paged
+ *                        (kv_lens counts suffix tokens only; 0 is allowed)
+ *  o [B, H, d] bf16, lse [B, H] fp32 (may be NULL): attention over prefix + suffix
+ *  workspace             >= attn_cascade_workspace_size(B, H, d, splits used)
+ *  prefix_len >= 0 (0: plain paged decode).  Supported as attn_decode_paged.
+ */
+attn_status_t attn_cascade_decode(const void *q, const void *prefix_k, const void *prefix_v, int prefix_len,
+                                  const void *k_pages, const void *v_pages, const int32_t *page_table,
+                                  const int32_t *kv_lens, void *o, float *lse,
+                                  int B, int H, int Hkv, int d, int page_size, int max_pages_per_seq,
+                                  int num_pages, float scale, int num_splits,
+                                  void *workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
  * merge_partials -- exact merge of per-chunk partial results.

@@ -37,6 +37,7 @@ from .attention import (  # noqa: F401
     merge_partials,
     finalize,
     decode_paged,
+    cascade_decode,
     gather_sequence,
     to_f64,
 )

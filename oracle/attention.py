@@ -14,6 +14,9 @@ Sources, by page title and section:
   online softmax" (per-tile update, skip tiles wholly in the future), "It is
   exact" (visited block-pair fractions), "The decode shape: splitting the keys"
   (the partial triple and merge_partials).
+* "3.4 Attention Kernels", "Paged and ragged layouts: FlashInfer" and
+  "Check your understanding" -- cascade attention: requests sharing a prefix
+  attend to the prefix followed by their own suffix.
 * "Multi-Head Attention to Flash Attention" (empirq) -- "Online Softmax
   Calculation" (the per-block update formulas; step 2 read as
   max(m_{j-1}, rowmax S_j), as its worked example does).
@@ -253,5 +256,31 @@ def decode_paged(q, k_pages, v_pages, page_table, kv_lens, *, scale: float, seqs
         for h in range(H):
             S = scale * (qf[b, h][None, :] @ Kb[h // g].T)    # [1, L]
             o, lse = _softmax_rows(S, Vb[h // g])
+            O[b, h], LSE[b, h] = o[0], lse[0]
+    return O, LSE
+
+
+def cascade_decode(q, prefix_k, prefix_v, k_pages, v_pages, page_table, kv_lens, *, scale: float, seqs=None):
+    """Decode for requests that share a prefix, by the plain definition.
+
+    Request b's query attends to the shared prefix's keys (prefix_k/prefix_v
+    [Hkv, prefix_len, d]) followed by its own suffix gathered through its page
+    table (kv_lens[b] tokens), with no mask.  Returns (O [B, H, d], LSE [B, H])
+    float64; rows of requests not in ``seqs`` stay (0, -inf).
+    """
+    B, H, d = q.shape
+    Hkv = k_pages.shape[1]
+    g = H // Hkv
+    Pk, Pv = to_f64(prefix_k), to_f64(prefix_v)
+    O = np.zeros((B, H, d))
+    LSE = np.full((B, H), -np.inf)
+    qf = to_f64(q)
+    for b in (range(B) if seqs is None else seqs):
+        Kb, Vb = gather_sequence(k_pages, v_pages, page_table, kv_lens, b)
+        for h in range(H):
+            keys = np.concatenate([Pk[h // g], Kb[h // g]], axis=0)
+            vals = np.concatenate([Pv[h // g], Vb[h // g]], axis=0)
+            S = scale * (qf[b, h][None, :] @ keys.T)
+            o, lse = _softmax_rows(S, vals)
             O[b, h], LSE[b, h] = o[0], lse[0]
     return O, LSE

@@ -384,3 +384,80 @@ def test_gqa_head_mapping_consecutive_heads_share():
     for h in range(H):
         np.testing.assert_array_equal(O[0, h], O[0, (h // 4) * 4])
     assert np.abs(O[0, 0] - O[0, 4]).max() > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# Cascade decode: shared prefix + own suffix
+# ---------------------------------------------------------------------------
+
+def test_cascade_equals_decode_with_prefix_pages():
+    """A page-aligned prefix stored as pages and prepended to every page table gives
+    the same result through decode_paged as through cascade_decode."""
+    rng = np.random.default_rng(61)
+    B, H, Hkv, d, ps = 3, 8, 2, 16, 4
+    npre = 3                                        # prefix of 3 pages = 12 tokens
+    lens = [0, 5, 9]
+    own = [-(-L // ps) for L in lens]
+    P = npre + sum(own)
+    kp = rng.standard_normal((P, Hkv, ps, d))
+    vp = rng.standard_normal((P, Hkv, ps, d))
+    q = rng.standard_normal((B, H, d))
+    own_table = np.zeros((B, max(own)), dtype=np.int64)
+    full_table = np.zeros((B, npre + max(own)), dtype=np.int64)
+    off = npre
+    for b, n in enumerate(own):
+        own_table[b, :n] = np.arange(off, off + n)
+        full_table[b, :npre] = np.arange(npre)
+        full_table[b, npre:npre + n] = np.arange(off, off + n)
+        off += n
+    prefix_k = kp[:npre].transpose(1, 0, 2, 3).reshape(Hkv, npre * ps, d)
+    prefix_v = vp[:npre].transpose(1, 0, 2, 3).reshape(Hkv, npre * ps, d)
+    Oc, Lc = oracle.cascade_decode(q, prefix_k, prefix_v, kp, vp, own_table, np.array(lens), scale=0.3)
+    Od, Ld = oracle.decode_paged(q, kp, vp, full_table, np.array(lens) + npre * ps, scale=0.3)
+    np.testing.assert_allclose(Oc, Od, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(Lc, Ld, rtol=0, atol=1e-12)
+
+
+def test_cascade_brute_force_and_merge_identity():
+    """Scalar brute force over prefix + suffix, and the merge of the two parts' states."""
+    rng = np.random.default_rng(62)
+    H, Hkv, d, ps, Lp, L = 2, 1, 4, 4, 5, 6
+    kp = rng.standard_normal((2, Hkv, ps, d))
+    vp = rng.standard_normal((2, Hkv, ps, d))
+    pk = rng.standard_normal((Hkv, Lp, d))
+    pv = rng.standard_normal((Hkv, Lp, d))
+    q = rng.standard_normal((1, H, d))
+    table = np.array([[1, 0]])
+    O, LSE = oracle.cascade_decode(q, pk, pv, kp, vp, table, np.array([L]), scale=0.7)
+    suffix_k = [kp[table[0, t // ps], 0, t % ps].tolist() for t in range(L)]
+    suffix_v = [vp[table[0, t // ps], 0, t % ps].tolist() for t in range(L)]
+    keys = pk[0].tolist() + suffix_k
+    vals = pv[0].tolist() + suffix_v
+    for h in range(H):
+        Ob, Lb = brute_attention([[[q[0, h].tolist()]]], [[keys]], [[vals]], False, 0.7)
+        np.testing.assert_allclose(O[0, h], np.array(Ob[0][0][0]), rtol=0, atol=1e-12)
+        assert abs(LSE[0, h] - Lb[0][0][0]) < 1e-12
+        sp = 0.7 * (pk[0] @ q[0, h])
+        ss = 0.7 * (np.array(suffix_k) @ q[0, h])
+        o2, l2 = oracle.finalize(*oracle.merge_partials([oracle.partial_state(sp, pv[0]),
+                                                         oracle.partial_state(ss, np.array(suffix_v))]))
+        np.testing.assert_allclose(o2, O[0, h], rtol=0, atol=1e-12)
+        assert abs(l2 - LSE[0, h]) < 1e-12
+
+
+@pytest.mark.parametrize("N,Nk", [(6, 3), (2, 9), (9, 2)])
+def test_cross_attention_bottom_right_mask_brute_force(N, Nk):
+    """Nq != Nk with the causal mask aligned to the last key; with Nq > Nk the first
+    Nq - Nk rows attend nothing (O = 0, LSE = -inf)."""
+    rng = np.random.default_rng(N * 10 + Nk)
+    Q = rng.standard_normal((1, 2, N, 4))
+    K = rng.standard_normal((1, 1, Nk, 4))
+    V = rng.standard_normal((1, 1, Nk, 4))
+    O, LSE = oracle.attention(Q, K, V, causal=True, scale=0.5)
+    Ob, Lb = brute_attention(Q.tolist(), K.tolist(), V.tolist(), True, 0.5)
+    np.testing.assert_allclose(O, np.array(Ob), rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(LSE), np.isneginf(np.array(Lb)))
+    fin = np.isfinite(LSE)
+    np.testing.assert_allclose(LSE[fin], np.array(Lb)[fin], rtol=0, atol=1e-12)
+    if N > Nk:
+        assert np.isneginf(LSE[0, :, : N - Nk]).all() and (O[0, :, : N - Nk] == 0).all()
