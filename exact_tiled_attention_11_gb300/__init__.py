@@ -17,6 +17,8 @@ from ._lib import (  # noqa: F401
     attn_device_error,
     attn_fwd,
     attn_fwd_cross,
+    attn_fwd_paged,
+    attn_fwd_varlen,
     attn_status_string,
     library_path,
     load_library,

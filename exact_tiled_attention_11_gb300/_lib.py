@@ -51,6 +51,11 @@ def load_library() -> ctypes.CDLL:
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp]
         lib.attn_fwd_cross.restype = i32
         lib.attn_fwd_cross.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp]
+        lib.attn_fwd_varlen.restype = i32
+        lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, vp]
+        lib.attn_fwd_paged.restype = i32
+        lib.attn_fwd_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                       i32, f32, vp]
         lib.attn_cascade_workspace_size.restype = sz
         lib.attn_cascade_workspace_size.argtypes = [i32, i32, i32, i32]
         lib.attn_cascade_decode.restype = i32
@@ -156,6 +161,56 @@ def attn_fwd_cross(q, k, v, o=None, lse=None, *, causal=False, scale=None, strea
     dt = ATTN_BF16 if q.dtype == torch.bfloat16 else ATTN_F32
     _check("attn_fwd_cross", lib.attn_fwd_cross(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Nq, Nk,
                                                 d, 1 if causal else 0, scale, dt, _stream(stream, q.device)))
+    return o, lse
+
+
+def attn_fwd_varlen(q, k, v, qo_indptr, kv_indptr, max_q_len, o=None, lse=None, *, causal=False, scale=None,
+                    stream=None):
+    """Ragged batch: q [total_q, H, d], k, v [total_k, Hkv, d] bf16; qo_indptr, kv_indptr
+    [B + 1] int32 (device); max_q_len the longest sequence's query count.
+    Returns (o [total_q, H, d] bf16, lse [total_q, H] fp32)."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 3)
+    _need(qo_indptr, "qo_indptr", torch.int32, 1)
+    _need(kv_indptr, "kv_indptr", torch.int32, 1)
+    total_q, H, d = q.shape
+    total_k, Hkv, _ = k.shape
+    B = qo_indptr.shape[0] - 1
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(total_q, H, dtype=torch.float32, device=q.device)
+    _check("attn_fwd_varlen", lib.attn_fwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(qo_indptr), _ptr(kv_indptr), B, H, Hkv, int(max_q_len),
+        total_q, total_k, d, 1 if causal else 0, (1.0 / d ** 0.5) if scale is None else float(scale),
+        _stream(stream, q.device)))
+    return o, lse
+
+
+def attn_fwd_paged(q, k_pages, v_pages, page_table, kv_lens, qo_indptr, max_q_len, o=None, lse=None, *,
+                   causal=True, scale=None, stream=None):
+    """Ragged query chunks q [total_q, H, d] (qo_indptr [B + 1]) against each sequence's
+    paged cache (k_pages, v_pages [P, Hkv, 16, d], page_table [B, max_pages], kv_lens [B]).
+    Returns (o [total_q, H, d] bf16, lse [total_q, H] fp32)."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_pages, "k_pages", torch.bfloat16, 4)
+    _need(v_pages, "v_pages", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    _need(kv_lens, "kv_lens", torch.int32, 1)
+    _need(qo_indptr, "qo_indptr", torch.int32, 1)
+    total_q, H, d = q.shape
+    P, Hkv, ps, _ = k_pages.shape
+    B = kv_lens.shape[0]
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(total_q, H, dtype=torch.float32, device=q.device)
+    _check("attn_fwd_paged", lib.attn_fwd_paged(
+        _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens), _ptr(qo_indptr), _ptr(o), _ptr(lse),
+        B, H, Hkv, int(max_q_len), total_q, d, ps, page_table.shape[1], P, 1 if causal else 0,
+        (1.0 / d ** 0.5) if scale is None else float(scale), _stream(stream, q.device)))
     return o, lse
 
 

@@ -206,6 +206,92 @@ attn_status_t attn_fwd_cross(const void *q, const void *k, const void *v, void *
   return fwd_impl(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, causal, scale, dtype, stream);
 }
 
+attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                              const int32_t *qo_indptr, const int32_t *kv_indptr, int B, int H, int Hkv,
+                              int max_q_len, int total_q, int total_k, int d, int causal, float scale,
+                              attn_stream_t stream) {
+  if (B < 0 || H < 0 || Hkv < 0 || max_q_len < 0 || total_q < 0 || total_k < 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || H == 0 || max_q_len == 0 || total_q == 0) return ATTN_OK;
+  if (Hkv == 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (q == nullptr || o == nullptr || qo_indptr == nullptr || kv_indptr == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (total_k > 0 && (k == nullptr || v == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
+    return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  PrefillMaps maps;
+  maps.q_rows_outer = true;
+  const void *kb = total_k > 0 ? k : q;
+  const void *vb = total_k > 0 ? v : q;
+  if (!make_map_3d(&maps.q, q, d, H, total_q, 1, 128) || !make_map_3d(&maps.k, kb, d, Hkv, total_k, 1, 128) ||
+      !make_map_3d(&maps.v, vb, d, Hkv, total_k, 1, 128))
+    return ATTN_ERR_CUDA;
+  PrefillOut out;
+  out.o = o;
+  out.lse = lse;
+  out.o_b = 0;
+  out.o_h = d;
+  out.o_r = static_cast<long long>(H) * d;
+  out.l_b = 0;
+  out.l_h = 1;
+  out.l_r = H;
+  attn::PrefillLayout lay;
+  lay.qo_indptr = qo_indptr;
+  lay.kv_indptr = kv_indptr;
+  lay.total_q = total_q;
+  lay.total_k = total_k;
+  cudaError_t e = attn::launch_prefill_bf16(maps, out, B, H, Hkv, max_q_len, 0, d, causal != 0, scale,
+                                            reinterpret_cast<cudaStream_t>(stream), lay);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,
+                             const int32_t *kv_lens, const int32_t *qo_indptr, void *o, float *lse, int B, int H,
+                             int Hkv, int max_q_len, int total_q, int d, int page_size, int max_pages_per_seq,
+                             int num_pages, int causal, float scale, attn_stream_t stream) {
+  if (B < 0 || H < 0 || Hkv < 0 || max_q_len < 0 || total_q < 0 || max_pages_per_seq < 0 || num_pages < 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || H == 0 || max_q_len == 0 || total_q == 0) return ATTN_OK;
+  if (Hkv == 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (q == nullptr || o == nullptr || qo_indptr == nullptr || kv_lens == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || (lse && !aligned16(lse))) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
+  const bool has_pages = max_pages_per_seq > 0 && num_pages > 0;
+  if (has_pages && (k_pages == nullptr || v_pages == nullptr || page_table == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (has_pages && (!aligned16(k_pages) || !aligned16(v_pages))) return ATTN_ERR_INVALID_ARG;
+  PrefillMaps maps;
+  maps.q_rows_outer = true;
+  const void *kb = has_pages ? k_pages : q;
+  const void *vb = has_pages ? v_pages : q;
+  const uint64_t planes = static_cast<uint64_t>(std::max(num_pages, 1)) * Hkv;
+  if (!make_map_3d(&maps.q, q, d, H, total_q, 1, 128) || !make_map_3d(&maps.k, kb, d, page_size, planes, page_size) ||
+      !make_map_3d(&maps.v, vb, d, page_size, planes, page_size))
+    return ATTN_ERR_CUDA;
+  PrefillOut out;
+  out.o = o;
+  out.lse = lse;
+  out.o_b = 0;
+  out.o_h = d;
+  out.o_r = static_cast<long long>(H) * d;
+  out.l_b = 0;
+  out.l_h = 1;
+  out.l_r = H;
+  attn::PrefillLayout lay;
+  lay.qo_indptr = qo_indptr;
+  lay.page_table = has_pages ? page_table : nullptr;
+  lay.kv_lens = kv_lens;
+  lay.max_pages = has_pages ? max_pages_per_seq : 0;
+  lay.num_pages = has_pages ? num_pages : 0;
+  lay.total_q = total_q;
+  // with no pages at all no page is read: every sequence has zero keys (and a
+  // positive kv_lens is recorded as beyond the table)
+  cudaError_t e = attn::launch_prefill_bf16(maps, out, B, H, Hkv, max_q_len, 0, d, causal != 0, scale,
+                                            reinterpret_cast<cudaStream_t>(stream), lay);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 size_t attn_decode_workspace_size(int B, int H, int d, int max_splits) {
   if (B <= 0 || H <= 0 || d <= 0 || max_splits <= 0) return 0;
   return decode_ws_bytes(B, H, d, max_splits);

@@ -36,13 +36,35 @@ cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, c
                                int Hkv, int Nq, int Nk, int d, bool causal, float scale, cudaStream_t stream);
 
 // prefill_bf16.cu: Q, K, V through TMA maps whose dimensions are (d, rows, B * heads);
-// with q_rows_outer the Q map is (d, B * H, rows) instead (box (64, 1, 128)).
+// with q_rows_outer the Q map is (d, heads, rows) instead (box (64, 1, 128)): ragged
+// queries [tokens, H, d], or q [B, H, d] read as one batch of B rows.
 struct PrefillMaps {
   CUtensorMap q, k, v;
   bool q_rows_outer = false;
 };
+// Per-sequence layout, chosen by which pointers are set (one kernel instance each):
+//  * dense (all null): sequence b's rows are rows [0, Nq) / [0, Nk) of plane b;
+//  * ragged (qo_indptr and kv_indptr): queries are rows [qo_indptr[b], qo_indptr[b+1])
+//    and keys rows [kv_indptr[b], kv_indptr[b+1]) of token-major tensors; the K/V maps
+//    are (d, Hkv, total_k) like a rows-outer Q map, and Nq is the longest sequence's
+//    query count (it sizes the grid);
+//  * paged (qo_indptr and kv_lens): ragged queries; keys are the kv_lens[b] tokens
+//    gathered through page_table[b, :] from a pool of num_pages pages of 16 tokens,
+//    the K/V maps spanning the pool as (d, 16, num_pages * Hkv).  With max_pages 0 no
+//    page is ever read (page_table may then be null).
+struct PrefillLayout {
+  const int32_t *qo_indptr = nullptr;
+  const int32_t *kv_indptr = nullptr;
+  const int32_t *page_table = nullptr;
+  const int32_t *kv_lens = nullptr;
+  int max_pages = 0;
+  int num_pages = 0;
+  int total_q = 0;  // rows of q / o (bounds every indptr range)
+  int total_k = 0;  // rows of k / v
+};
 cudaError_t launch_prefill_bf16(const PrefillMaps &maps, const PrefillOut &out, int B, int H, int Hkv, int Nq,
-                                int Nk, int d, bool causal, float scale, cudaStream_t stream);
+                                int Nk, int d, bool causal, float scale, cudaStream_t stream,
+                                const PrefillLayout &layout = PrefillLayout());
 
 // Per-translation-unit device error words (see common.cuh).
 cudaError_t device_error_decode(unsigned int *value, bool clear);

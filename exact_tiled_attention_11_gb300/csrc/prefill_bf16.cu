@@ -150,11 +150,19 @@ __device__ __forceinline__ void rescale_o_chunk(uint32_t taddr, float corr) {
   tc05::tmem_st_x32(taddr, r);
 }
 
-template <int D>
+// Where each sequence's rows live: one dense block per (batch, head), ragged
+// (indptr offsets into token-major q/k/v), or ragged queries against a paged cache.
+enum { kDense = 0, kRagged = 1, kPaged = 2 };
+
+template <int D, int kLay>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const PrefillOut out, int B, int H, int Hkv,
-                        int Nq, int Nk, int causal, float scale_log2, int q_rows_outer) {
+                        const __grid_constant__ CUtensorMap tm_v, const PrefillOut out, const PrefillLayout lay,
+                        int B, int H, int Hkv, int Nq_max, int Nk_dense, int causal, float scale_log2,
+                        int q_rows_outer) {
+  constexpr bool kRaggedQ = kLay != kDense;  // query offsets from qo_indptr
+  constexpr bool kRaggedK = kLay == kRagged;  // key offsets from kv_indptr (rows-outer K/V maps)
+  constexpr bool kPagedK = kLay == kPaged;    // keys gathered page by page
   using Smem = PrefillSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -163,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   // ---- which (query-tile pair, batch, head): heaviest causal pairs first
-  const int n_pairs = (Nq + 2 * BM - 1) / (2 * BM);
+  const int n_pairs = (Nq_max + 2 * BM - 1) / (2 * BM);
   const int bh_count = B * H;
   const int rank = blockIdx.x / bh_count;
   const int bh = blockIdx.x % bh_count;
@@ -171,6 +179,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / H;
   const int h = bh % H;
   const int kvh = h / (H / Hkv);
+  // ---- this sequence's query rows and keys
+  // A sequence whose offsets leave [0, total) or exceed the host's max_q_len is
+  // not computed (its rows stay unwritten) and sets BAD_LENGTH.  Every thread
+  // reads the same values, so the whole CTA leaves together.
+  int Nq = Nq_max, Nk = Nk_dense, q_base = 0, k_base = 0;
+  bool bad = false;
+  if (kRaggedQ) {
+    q_base = lay.qo_indptr[b];
+    Nq = lay.qo_indptr[b + 1] - q_base;
+    bad |= q_base < 0 || Nq < 0 || Nq > Nq_max || static_cast<long long>(q_base) + Nq > lay.total_q;
+  }
+  if (kRaggedK) {
+    k_base = lay.kv_indptr[b];
+    Nk = lay.kv_indptr[b + 1] - k_base;
+    bad |= k_base < 0 || Nk < 0 || static_cast<long long>(k_base) + Nk > lay.total_k;
+  }
+  if (bad) {
+    if (t == 0 && threadIdx.x == 0) record_device_error(ATTN_DEVERR_BAD_LENGTH);
+    return;
+  }
+  if (kPagedK) {
+    Nk = lay.kv_lens[b];
+    if (Nk < 0 || Nk > lay.max_pages * 16) {  // beyond the table: clamped, as in paged decode
+      if (t == 0 && threadIdx.x == 0) record_device_error(ATTN_DEVERR_BAD_PAGE);
+      Nk = max(0, min(Nk, lay.max_pages * 16));
+    }
+  }
+  if (2 * t * BM >= Nq) return;  // this pair lies past the sequence's queries
+  const int q_plane = kRaggedQ ? h : b * H + h;
+  const int kv_plane = kRaggedK ? kvh : b * Hkv + kvh;
   const int row0[2] = {2 * t * BM, (2 * t + 1) * BM};
   const bool has_b = row0[1] < Nq;
   const int n_kt_all = (Nk + BN - 1) / BN;
@@ -216,6 +254,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 56 per thread and the two softmax warpgroups take 224:
   // 128 x 56 + 256 x 224 = 64,512, exactly the launch's allocation.
   if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+  // Key tile j of this sequence into shared memory: one box per 64 columns, or,
+  // paged, eight 16-token pages per 64 columns (a page id past the sequence or
+  // outside the pool reads as zeros: TMA fills out-of-range boxes).
+  auto load_kv_tile = [&](uint32_t dst, const CUtensorMap *map, uint32_t bar, int j, uint64_t policy,
+                          const int (&pages)[8]) {
+#pragma unroll
+    for (int x = 0; x < D / 64; ++x) {
+      if (!kPagedK) {
+        if (kRaggedK)
+          tma_load_3d_hint(dst + x * kBoxBytes, map, bar, x * 64, kv_plane, k_base + j * BN, policy);
+        else
+          tma_load_3d_hint(dst + x * kBoxBytes, map, bar, x * 64, j * BN, kv_plane, policy);
+      } else {
+#pragma unroll
+        for (int pg = 0; pg < 8; ++pg)
+          tma_load_3d_hint(dst + x * kBoxBytes + pg * 16 * 128, map, bar, x * 64, 0, pages[pg] * Hkv + kvh, policy);
+      }
+    }
+  };
+  // page ids of key tile j (paged layout; -1 past the sequence's pages)
+  auto tile_pages = [&](int j, int (&pages)[8]) {
+    const int pages_b = (Nk + 15) / 16;
+#pragma unroll
+    for (int pg = 0; pg < 8; ++pg) {
+      const int i = j * 8 + pg;
+      int id = -1;
+      if (kPagedK && i < pages_b) {
+        id = lay.page_table[static_cast<size_t>(b) * lay.max_pages + i];
+        if (id < 0 || id >= lay.num_pages) {
+          record_device_error(ATTN_DEVERR_BAD_PAGE);
+          id = -1;
+        }
+      }
+      pages[pg] = id;
+    }
+  };
   if (warp == 0) {
     // ================================================================ TMA: Q and K
     if (lane == 0) {
@@ -228,18 +302,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < (has_b ? 2 : 1); ++c)
 #pragma unroll
         for (int x = 0; x < D / 64; ++x)
-          // Q map dimensions: (d, rows, B * H), or (d, B * H, rows) when the query rows are the outer dimension
-          tma_load_3d_hint(smem_u32(sm.q[c]) + x * kBoxBytes, &tm_q, qbar, x * 64, q_rows_outer ? b * H + h : row0[c],
-                           q_rows_outer ? row0[c] : b * H + h, once);
+          // Q map dimensions: (d, rows, planes), or (d, planes, rows) when the query rows are the outer dimension
+          tma_load_3d_hint(smem_u32(sm.q[c]) + x * kBoxBytes, &tm_q, qbar, x * 64,
+                           q_rows_outer ? q_plane : q_base + row0[c], q_rows_outer ? q_base + row0[c] : q_plane, once);
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int ks = j % kKStages;
         if (j >= kKStages && !mbar_wait(smem_u32(&sm.k_empty[ks]), ((j / kKStages) - 1) & 1, &sm.abort)) break;
+        int pages[8];
+        tile_pages(j, pages);
         const uint32_t kbar = smem_u32(&sm.k_full[ks]);
         mbar_arrive_expect_tx(kbar, Smem::kTileBytes);
-#pragma unroll
-        for (int x = 0; x < D / 64; ++x)
-          tma_load_3d_hint(smem_u32(sm.k[ks]) + x * kBoxBytes, &tm_k, kbar, x * 64, j * BN, b * Hkv + kvh, keep);
+        load_kv_tile(smem_u32(sm.k[ks]), &tm_k, kbar, j, keep, pages);
         ++issued;
       }
       // drain: every issued copy must land before the CTA's shared memory is released
@@ -257,12 +331,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t keep = l2_policy_evict_last();
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
+        int pages[8];
+        tile_pages(j, pages);  // before the wait: the ids do not depend on the stage
         if (j >= 1 && !mbar_wait(smem_u32(&sm.v_empty), (j - 1) & 1, &sm.abort)) break;
         const uint32_t vbar = smem_u32(&sm.v_full);
         mbar_arrive_expect_tx(vbar, Smem::kTileBytes);
-#pragma unroll
-        for (int x = 0; x < D / 64; ++x)
-          tma_load_3d_hint(smem_u32(sm.v) + x * kBoxBytes, &tm_v, vbar, x * 64, j * BN, b * Hkv + kvh, keep);
+        load_kv_tile(smem_u32(sm.v), &tm_v, vbar, j, keep, pages);
         ++issued;
       }
       if (issued > 0) mbar_wait(smem_u32(&sm.v_full), (issued - 1) & 1, nullptr);
@@ -476,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t inv2 = f2(inv, inv);
         const bool store = q_row < Nq;
         __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(out.o) + b * out.o_b + h * out.o_h +
-                              static_cast<long long>(store ? q_row : 0) * out.o_r;
+                              static_cast<long long>(q_base + (store ? q_row : 0)) * out.o_r;
 #pragma unroll
         for (int q4 = 0; q4 < D / 32; ++q4) {
           uint32_t orr[32];
@@ -497,16 +571,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (store && out.lse != nullptr)
-          out.lse[b * out.l_b + h * out.l_h + static_cast<long long>(q_row) * out.l_r] =
+          out.lse[b * out.l_b + h * out.l_h + static_cast<long long>(q_base + q_row) * out.l_r] =
               (l > 0.f) ? m_ref * kLn2 + logf(l) : -INFINITY;
       }
     } else if (n_c == 0 && q_row < Nq) {
       // a tile whose rows attend no key (causal, Nq > Nk): O = 0, LSE = -inf
       uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(out.o) + b * out.o_b + h * out.o_h +
-                                             static_cast<long long>(q_row) * out.o_r);
+                                             static_cast<long long>(q_base + q_row) * out.o_r);
 #pragma unroll
       for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
-      if (out.lse != nullptr) out.lse[b * out.l_b + h * out.l_h + static_cast<long long>(q_row) * out.l_r] = -INFINITY;
+      if (out.lse != nullptr)
+        out.lse[b * out.l_b + h * out.l_h + static_cast<long long>(q_base + q_row) * out.l_r] = -INFINITY;
     }
   }
 
@@ -518,21 +593,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
-cudaError_t launch_d(const PrefillMaps &maps, const PrefillOut &out, int B, int H, int Hkv, int Nq, int Nk,
-                     bool causal, float scale, cudaStream_t stream) {
+template <int D, int kLay>
+cudaError_t launch_d(const PrefillMaps &maps, const PrefillOut &out, const PrefillLayout &lay, int B, int H, int Hkv,
+                     int Nq, int Nk, bool causal, float scale, cudaStream_t stream) {
   // One CTA per SM: the kernel holds all 512 tensor-memory columns.
   const size_t smem = std::max<size_t>(sizeof(PrefillSmem<D>) + 1024, 120 * 1024);
-  auto kern = prefill_bf16_kernel<D>;
+  auto kern = prefill_bf16_kernel<D, kLay>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long n_pairs = (Nq + 2 * BM - 1) / (2 * BM);
   const long long blocks = n_pairs * B * H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(maps.q, maps.k, maps.v, out, B, H, Hkv, Nq, Nk,
-                                                                   causal ? 1 : 0, scale * kLog2e,
+  kern<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(maps.q, maps.k, maps.v, out, lay, B, H, Hkv, Nq,
+                                                                   Nk, causal ? 1 : 0, scale * kLog2e,
                                                                    maps.q_rows_outer ? 1 : 0);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_layout(const PrefillMaps &maps, const PrefillOut &out, const PrefillLayout &lay, int B, int H,
+                          int Hkv, int Nq, int Nk, bool causal, float scale, cudaStream_t stream) {
+  if (lay.kv_lens != nullptr) return launch_d<D, kPaged>(maps, out, lay, B, H, Hkv, Nq, Nk, causal, scale, stream);
+  if (lay.kv_indptr != nullptr) return launch_d<D, kRagged>(maps, out, lay, B, H, Hkv, Nq, Nk, causal, scale, stream);
+  return launch_d<D, kDense>(maps, out, lay, B, H, Hkv, Nq, Nk, causal, scale, stream);
 }
 
 }  // namespace
@@ -540,9 +623,10 @@ cudaError_t launch_d(const PrefillMaps &maps, const PrefillOut &out, int B, int 
 ATTN_DEFINE_ERROR_ACCESSOR(device_error_prefill_bf16)
 
 cudaError_t launch_prefill_bf16(const PrefillMaps &maps, const PrefillOut &out, int B, int H, int Hkv, int Nq,
-                                int Nk, int d, bool causal, float scale, cudaStream_t stream) {
-  if (d == 64) return launch_d<64>(maps, out, B, H, Hkv, Nq, Nk, causal, scale, stream);
-  return launch_d<128>(maps, out, B, H, Hkv, Nq, Nk, causal, scale, stream);
+                                int Nk, int d, bool causal, float scale, cudaStream_t stream,
+                                const PrefillLayout &layout) {
+  if (d == 64) return launch_layout<64>(maps, out, layout, B, H, Hkv, Nq, Nk, causal, scale, stream);
+  return launch_layout<128>(maps, out, layout, B, H, Hkv, Nq, Nk, causal, scale, stream);
 }
 
 }  // namespace attn

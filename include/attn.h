@@ -94,6 +94,60 @@ attn_status_t attn_fwd_cross(const void *q, const void *k, const void *v, void *
                              attn_dtype_t dtype, attn_stream_t stream);
 
 /*
+ * attn_fwd_varlen -- exact attention over a batch of sequences of different
+ * lengths packed without padding (ragged tensors).
+ *
+ * Follows "3.4 Attention Kernels", "Paged and ragged layouts: FlashInfer":
+ * all sequences' tokens are concatenated and an offsets array (indptr) marks
+ * where each sequence starts.  Sequence b's queries are rows
+ * [qo_indptr[b], qo_indptr[b+1]) of q and its keys/values rows
+ * [kv_indptr[b], kv_indptr[b+1]) of k and v; each sequence is attended on its
+ * own with the tcgen05 prefill kernel (same algorithm as attn_fwd).  With
+ * causal = 1 the mask is aligned to each sequence's last key (query row i of
+ * a sequence with Lq queries and Lk keys attends keys j <= i + Lk - Lq).
+ *
+ *  q         [total_q, H, d]    bf16    k, v [total_k, Hkv, d] bf16
+ *  o         [total_q, H, d]    bf16    lse  [total_q, H] fp32 (may be NULL)
+ *  qo_indptr, kv_indptr  [B + 1] int32, device, non-decreasing, within [0, total_q] / [0, total_k]
+ *  max_q_len  the longest sequence's query count (sizes the grid on the host)
+ *  d in {64, 128}.
+ * The offsets stay on the device (no copy, so the call can be graph-captured);
+ * the kernel checks them: a sequence with more than max_q_len queries, or whose
+ * offsets leave those ranges, is not computed (its rows of o and lse are left
+ * unwritten) and sets ATTN_DEVERR_BAD_LENGTH in attn_device_error.
+ */
+attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                              const int32_t *qo_indptr, const int32_t *kv_indptr, int B, int H, int Hkv,
+                              int max_q_len, int total_q, int total_k, int d, int causal, float scale,
+                              attn_stream_t stream);
+
+/*
+ * attn_fwd_paged -- prefill of ragged query chunks against a paged KV cache
+ * (continuous batching: new tokens of several sequences in one launch).
+ *
+ * Follows "3.4 Attention Kernels", "Paged and ragged layouts: FlashInfer"
+ * (ragged queries through indptr; K/V gathered through the block table and
+ * the sequence lengths).  Sequence b's queries are rows
+ * [qo_indptr[b], qo_indptr[b+1]) of q; its keys are the kv_lens[b] tokens of
+ * its pages, with the query chunk being the last tokens of the sequence:
+ * with causal = 1, query row i of a chunk of Lq rows attends keys
+ * j <= i + kv_lens[b] - Lq.  The K/V tiles are gathered page by page by TMA.
+ *
+ *  q          [total_q, H, d] bf16     o [total_q, H, d] bf16   lse [total_q, H] fp32 (nullable)
+ *  k_pages, v_pages, page_table, kv_lens, num_pages: as attn_decode_paged (page_size 16;
+ *             bad page ids and kv_lens values beyond the table are handled the same way)
+ *  qo_indptr  [B + 1] int32, device, checked as in attn_fwd_varlen (with total_q);
+ *  max_q_len  as attn_fwd_varlen;  d in {64, 128}.
+ * Each 128-key tile is loaded as whole 16-token pages, so the slots past
+ * kv_lens[b] in a sequence's last page are read and multiplied by zero
+ * weights: they must hold finite values (stale tokens or zeros, not NaN/Inf).
+ */
+attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,
+                             const int32_t *kv_lens, const int32_t *qo_indptr, void *o, float *lse,
+                             int B, int H, int Hkv, int max_q_len, int total_q, int d, int page_size,
+                             int max_pages_per_seq, int num_pages, int causal, float scale, attn_stream_t stream);
+
+/*
  * attn_decode_workspace_size -- bytes of device workspace attn_decode_paged
  * needs for up to max_splits partial results per (sequence, query head):
  * fp32 m and l [B, H, max_splits] and fp32 o~ [B, H, max_splits, d], each
@@ -122,6 +176,8 @@ size_t attn_decode_workspace_size(int B, int H, int d, int max_splits);
  *  num_pages   P, the pool size (the tensor-map extent).  A page id outside [0, P)
  *              reads as zeros (TMA fills out-of-range boxes) and is recorded as
  *              ATTN_DEVERR_BAD_PAGE; so is a kv_lens value beyond the table.
+ *              Slots past kv_lens[b] in a sequence's last page are read and
+ *              weighted by zero: they must hold finite values.
  *  num_splits  upper bound on the key chunks per sequence; <= 0 picks one from
  *              B, Hkv, max_pages_per_seq and the SM count.  The chunk is
  *              ceil(max_pages_per_seq / num_splits) pages; sequence b uses
@@ -250,6 +306,7 @@ attn_status_t attn_device_error(uint32_t *code, int clear);
 #define ATTN_DEVERR_WAIT_TIMEOUT 0x1u   /* a pipeline wait gave up after its iteration limit */
 #define ATTN_DEVERR_BAD_PAGE     0x2u   /* a page id outside [0, num_pages) was skipped */
 #define ATTN_DEVERR_TMEM_ALLOC   0x4u   /* tensor memory allocation returned an unusable address */
+#define ATTN_DEVERR_BAD_LENGTH   0x8u   /* a ragged sequence's offsets were out of range or exceeded max_q_len */
 
 #ifdef __cplusplus
 }

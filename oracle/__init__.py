@@ -38,6 +38,8 @@ from .attention import (  # noqa: F401
     finalize,
     decode_paged,
     cascade_decode,
+    varlen_attention,
+    paged_prefill,
     gather_sequence,
     to_f64,
 )

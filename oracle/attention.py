@@ -16,7 +16,8 @@ Sources, by page title and section:
   (the partial triple and merge_partials).
 * "3.4 Attention Kernels", "Paged and ragged layouts: FlashInfer" and
   "Check your understanding" -- cascade attention: requests sharing a prefix
-  attend to the prefix followed by their own suffix.
+  attend to the prefix followed by their own suffix; ragged tensors (tokens
+  concatenated, an indptr of sequence starts) and paged K/V for prefill.
 * "Multi-Head Attention to Flash Attention" (empirq) -- "Online Softmax
   Calculation" (the per-block update formulas; step 2 read as
   max(m_{j-1}, rowmax S_j), as its worked example does).
@@ -283,4 +284,55 @@ def cascade_decode(q, prefix_k, prefix_v, k_pages, v_pages, page_table, kv_lens,
             S = scale * (qf[b, h][None, :] @ keys.T)
             o, lse = _softmax_rows(S, vals)
             O[b, h], LSE[b, h] = o[0], lse[0]
+    return O, LSE
+
+
+def varlen_attention(q, k, v, qo_indptr, kv_indptr, *, causal: bool, scale: float):
+    """Ragged batch by the plain definition, one sequence at a time.
+
+    q [total_q, H, d], k/v [total_k, Hkv, d]; sequence b owns query rows
+    [qo_indptr[b], qo_indptr[b+1]) and key rows [kv_indptr[b], kv_indptr[b+1]).
+    The causal mask is aligned to each sequence's last key.  Returns
+    (O [total_q, H, d], LSE [total_q, H]) float64.
+    """
+    qf, kf, vf = to_f64(q), to_f64(k), to_f64(v)
+    total_q, H, d = qf.shape
+    Hkv = kf.shape[1]
+    O = np.zeros((total_q, H, d))
+    LSE = np.full((total_q, H), -np.inf)
+    qo = [int(x) for x in qo_indptr]
+    kvp = [int(x) for x in kv_indptr]
+    for b in range(len(qo) - 1):
+        qs, qe, ks, ke = qo[b], qo[b + 1], kvp[b], kvp[b + 1]
+        if qe == qs:
+            continue
+        Qb = qf[qs:qe].transpose(1, 0, 2)[None]          # [1, H, Lq, d]
+        Kb = kf[ks:ke].transpose(1, 0, 2)[None]          # [1, Hkv, Lk, d]
+        Vb = vf[ks:ke].transpose(1, 0, 2)[None]
+        Ob, Lb = attention(Qb, Kb, Vb, causal=causal, scale=scale)
+        O[qs:qe] = Ob[0].transpose(1, 0, 2)
+        LSE[qs:qe] = Lb[0].T
+    return O, LSE
+
+
+def paged_prefill(q, k_pages, v_pages, page_table, kv_lens, qo_indptr, *, causal: bool, scale: float):
+    """Ragged query chunks against each sequence's paged cache, by the plain definition.
+
+    Sequence b's queries (rows [qo_indptr[b], qo_indptr[b+1]) of q [total_q, H, d])
+    are the last tokens of its kv_lens[b] keys, gathered token by token through its
+    page table.  Returns (O [total_q, H, d], LSE [total_q, H]) float64.
+    """
+    qf = to_f64(q)
+    total_q, H, d = qf.shape
+    O = np.zeros((total_q, H, d))
+    LSE = np.full((total_q, H), -np.inf)
+    qo = [int(x) for x in qo_indptr]
+    for b in range(len(qo) - 1):
+        qs, qe = qo[b], qo[b + 1]
+        if qe == qs:
+            continue
+        Kb, Vb = gather_sequence(k_pages, v_pages, page_table, kv_lens, b)   # [Hkv, L, d]
+        Ob, Lb = attention(qf[qs:qe].transpose(1, 0, 2)[None], Kb[None], Vb[None], causal=causal, scale=scale)
+        O[qs:qe] = Ob[0].transpose(1, 0, 2)
+        LSE[qs:qe] = Lb[0].T
     return O, LSE

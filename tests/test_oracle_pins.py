@@ -461,3 +461,52 @@ def test_cross_attention_bottom_right_mask_brute_force(N, Nk):
     np.testing.assert_allclose(LSE[fin], np.array(Lb)[fin], rtol=0, atol=1e-12)
     if N > Nk:
         assert np.isneginf(LSE[0, :, : N - Nk]).all() and (O[0, :, : N - Nk] == 0).all()
+
+
+# ---------------------------------------------------------------------------
+# Ragged batches (indptr) and paged prefill
+# ---------------------------------------------------------------------------
+
+def test_varlen_equal_lengths_is_dense_attention():
+    rng = np.random.default_rng(71)
+    B, H, Hkv, N, d = 3, 4, 2, 9, 8
+    Q = rng.standard_normal((B, H, N, d))
+    K = rng.standard_normal((B, Hkv, N, d))
+    V = rng.standard_normal((B, Hkv, N, d))
+    indptr = np.arange(B + 1) * N
+    q = Q.transpose(0, 2, 1, 3).reshape(B * N, H, d)
+    k = K.transpose(0, 2, 1, 3).reshape(B * N, Hkv, d)
+    v = V.transpose(0, 2, 1, 3).reshape(B * N, Hkv, d)
+    for causal in (False, True):
+        O, LSE = oracle.attention(Q, K, V, causal=causal, scale=0.4)
+        Ov, Lv = oracle.varlen_attention(q, k, v, indptr, indptr, causal=causal, scale=0.4)
+        np.testing.assert_allclose(Ov, O.transpose(0, 2, 1, 3).reshape(B * N, H, d), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(Lv, LSE.transpose(0, 2, 1).reshape(B * N, H), rtol=0, atol=1e-12)
+
+
+def test_paged_prefill_brute_force():
+    """Query chunks that are the last tokens of each sequence, keys gathered page by page."""
+    rng = np.random.default_rng(72)
+    H, Hkv, d, ps = 2, 1, 4, 4
+    kv_lens = [6, 9]
+    q_lens = [2, 9]
+    pages = [-(-L // ps) for L in kv_lens]
+    P = sum(pages)
+    perm = rng.permutation(P)
+    table = np.zeros((2, max(pages)), dtype=np.int64)
+    table[0, :pages[0]] = perm[:pages[0]]
+    table[1, :pages[1]] = perm[pages[0]:]
+    kp = rng.standard_normal((P, Hkv, ps, d))
+    vp = rng.standard_normal((P, Hkv, ps, d))
+    qo = np.array([0, 2, 11])
+    q = rng.standard_normal((11, H, d))
+    O, LSE = oracle.paged_prefill(q, kp, vp, table, np.array(kv_lens), qo, causal=True, scale=0.6)
+    for b in range(2):
+        L, Lq = kv_lens[b], q_lens[b]
+        keys = [[kp[table[b, t // ps], 0, t % ps, e] for e in range(d)] for t in range(L)]
+        vals = [[vp[table[b, t // ps], 0, t % ps, e] for e in range(d)] for t in range(L)]
+        rows = q[qo[b]:qo[b + 1]]
+        Qb = [[rows[:, h].tolist() for h in range(H)]]
+        Ob, Lb = brute_attention(Qb, [[keys]], [[vals]], True, 0.6)
+        np.testing.assert_allclose(O[qo[b]:qo[b + 1]], np.array(Ob[0]).transpose(1, 0, 2), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(LSE[qo[b]:qo[b + 1]], np.array(Lb[0]).T, rtol=0, atol=1e-12)
