@@ -161,3 +161,9 @@ def decode_inputs(B, H, Hkv, d, page_size, len_lo, len_hi, seed=0, kv_lens=None)
 def decode_inputs_for(cfg: DecodeConfig, seed=0, kv_lens=None, B=None):
     return decode_inputs(cfg.B if B is None else B, cfg.H, cfg.Hkv, cfg.d, cfg.page_size,
                          cfg.len_lo, cfg.len_hi, seed, kv_lens)
+
+
+def fp8_signs(d: int, seed: int = 0) -> torch.Tensor:
+    """The random +-1 diagonal of the FP8 path's orthogonal transform (fp32, seeded)."""
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randint(0, 2, (d,), generator=g) * 2 - 1).to(torch.float32)

@@ -22,12 +22,22 @@ that it can be checked against the pages by eye:
                           merge rule.
 * ``decode_paged``     -- one query token per sequence against a paged, ragged
                           KV cache gathered through a page table.
+* ``cascade_decode``, ``varlen_attention``, ``paged_prefill`` -- a shared prefix
+                          plus own suffix; ragged (indptr) batches; ragged
+                          query chunks against a paged cache.
+* ``fp8`` (submodule)  -- FP8 attention's inputs: the random orthogonal
+                          (Hadamard) transform of Q and K, block quantisation to
+                          e4m3 with one scale per 128-row block, and the exact
+                          attention of the dequantised blocks.
 
 Pins (``tests/test_oracle_pins.py``, ``-m "not gpu"``): the worked examples the
 pages print, a scalar pure-Python brute force on tiny inputs, closed forms
 (K = 0, one key), invariants (block-shape independence, partition/merge
 independence, convex combination, no overflow at large scores) and the causal
-block-pair counts the pages report.  No function here is unpinned.
+block-pair counts the pages report; ``tests/test_oracle_fp8.py`` pins the FP8
+part against PyTorch's e4m3 conversion, scipy's Hadamard matrix, orthogonality,
+a scalar brute force and the quantisation error bound.  No function here is
+unpinned.
 """
 from .attention import (  # noqa: F401
     attention,
@@ -43,3 +53,4 @@ from .attention import (  # noqa: F401
     gather_sequence,
     to_f64,
 )
+from . import fp8  # noqa: F401
