@@ -8,6 +8,7 @@ from ._lib import (  # noqa: F401
     ATTN_BF16,
     ATTN_F32,
     AttnError,
+    Fp8Inputs,
     attn_cascade_decode,
     attn_cascade_workspace_size,
     attn_decode_max_splits,
@@ -15,8 +16,11 @@ from ._lib import (  # noqa: F401
     attn_decode_paged_noalloc,
     attn_decode_workspace_size,
     attn_device_error,
+    attn_fp8_padded_keys,
+    attn_fp8_quantize,
     attn_fwd,
     attn_fwd_cross,
+    attn_fwd_fp8,
     attn_fwd_paged,
     attn_fwd_varlen,
     attn_status_string,

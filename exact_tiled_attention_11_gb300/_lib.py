@@ -12,6 +12,7 @@ from __future__ import annotations
 import ctypes
 import os
 import threading
+from typing import NamedTuple
 
 import torch
 
@@ -73,6 +74,12 @@ def load_library() -> ctypes.CDLL:
                                                   i32, vp]
         lib.merge_partials.restype = i32
         lib.merge_partials.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, i32, vp, vp]
+        lib.attn_fp8_padded_keys.restype = i32
+        lib.attn_fp8_padded_keys.argtypes = [i32]
+        lib.attn_fp8_quantize.restype = i32
+        lib.attn_fp8_quantize.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
+        lib.attn_fwd_fp8.restype = i32
+        lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_status_string.argtypes = [i32]
         lib.attn_device_error.restype = i32
@@ -211,6 +218,77 @@ def attn_fwd_paged(q, k_pages, v_pages, page_table, kv_lens, qo_indptr, max_q_le
         _ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(kv_lens), _ptr(qo_indptr), _ptr(o), _ptr(lse),
         B, H, Hkv, int(max_q_len), total_q, d, ps, page_table.shape[1], P, 1 if causal else 0,
         (1.0 / d ** 0.5) if scale is None else float(scale), _stream(stream, q.device)))
+    return o, lse
+
+
+class Fp8Inputs(NamedTuple):
+    """FP8 blocks of one attention call (see attn_fp8_quantize in include/attn.h)."""
+    q8: torch.Tensor        # [B, H, Nq, 128] uint8 e4m3 codes of q M
+    k8: torch.Tensor        # [B, Hkv, Nk, 128] uint8 e4m3 codes of k M
+    v8t: torch.Tensor       # [B, Hkv, 128, Nk_pad] uint8 e4m3 codes of v, transposed
+    q_scale: torch.Tensor   # [B, H, ceil(Nq / 128)] fp32
+    k_scale: torch.Tensor   # [B, Hkv, ceil(Nk / 128)] fp32
+    v_scale: torch.Tensor   # [B, Hkv, ceil(Nk / 128)] fp32
+
+
+def attn_fp8_padded_keys(Nk: int) -> int:
+    return int(load_library().attn_fp8_padded_keys(Nk))
+
+
+def attn_fp8_quantize(q, k, v, signs=None, out: Fp8Inputs = None, *, stream=None) -> Fp8Inputs:
+    """Block-quantise bf16 q [B, H, Nq, 128], k, v [B, Hkv, Nk, 128] to e4m3, after the
+    orthogonal transform diag(signs) H / sqrt(128) of q and k (signs [128] fp32 +-1 on the
+    device, or None for no transform).  Allocates the outputs unless ``out`` is given."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if k.shape != (B, Hkv, Nk, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, Nk, d] matching q")
+    if signs is not None:
+        _need(signs, "signs", torch.float32, 1)
+        if signs.numel() != d:
+            raise ValueError(f"signs must hold {d} values")
+    if out is None:
+        dev = q.device
+        nq, nk = -(-Nq // 128), -(-Nk // 128)
+        out = Fp8Inputs(torch.empty(B, H, Nq, d, dtype=torch.uint8, device=dev),
+                        torch.empty(B, Hkv, Nk, d, dtype=torch.uint8, device=dev),
+                        torch.empty(B, Hkv, d, attn_fp8_padded_keys(Nk), dtype=torch.uint8, device=dev),
+                        torch.empty(B, H, nq, dtype=torch.float32, device=dev),
+                        torch.empty(B, Hkv, nk, dtype=torch.float32, device=dev),
+                        torch.empty(B, Hkv, nk, dtype=torch.float32, device=dev))
+    _check("attn_fp8_quantize", lib.attn_fp8_quantize(
+        _ptr(q), _ptr(k), _ptr(v), None if signs is None else _ptr(signs), _ptr(out.q8), _ptr(out.k8),
+        _ptr(out.v8t), _ptr(out.q_scale), _ptr(out.k_scale), _ptr(out.v_scale), B, H, Hkv, Nq, Nk, d,
+        _stream(stream, q.device)))
+    return out
+
+
+def attn_fwd_fp8(x: Fp8Inputs, o=None, lse=None, *, causal=False, scale=None, stream=None):
+    """Attention over FP8 blocks from attn_fp8_quantize.  Returns (o [B, H, Nq, 128] bf16,
+    lse [B, H, Nq] fp32)."""
+    lib = load_library()
+    _need(x.q8, "q8", torch.uint8, 4)
+    _need(x.k8, "k8", torch.uint8, 4)
+    _need(x.v8t, "v8t", torch.uint8, 4)
+    for t, n in ((x.q_scale, "q_scale"), (x.k_scale, "k_scale"), (x.v_scale, "v_scale")):
+        _need(t, n, torch.float32, 3)
+    B, H, Nq, d = x.q8.shape
+    Hkv, Nk = x.k8.shape[1], x.k8.shape[2]
+    if x.v8t.shape != (B, Hkv, d, attn_fp8_padded_keys(Nk)):
+        raise ValueError("v8t must be [B, Hkv, d, Nk_pad]")
+    if o is None:
+        o = torch.empty(B, H, Nq, d, dtype=torch.bfloat16, device=x.q8.device)
+    if lse is None:
+        lse = torch.empty(B, H, Nq, dtype=torch.float32, device=x.q8.device)
+    _need(o, "o", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    scale = (1.0 / d ** 0.5) if scale is None else float(scale)
+    _check("attn_fwd_fp8", lib.attn_fwd_fp8(
+        _ptr(x.q8), _ptr(x.k8), _ptr(x.v8t), _ptr(x.q_scale), _ptr(x.k_scale), _ptr(x.v_scale), _ptr(o), _ptr(lse),
+        B, H, Hkv, Nq, Nk, d, 1 if causal else 0, scale, _stream(stream, x.q8.device)))
     return o, lse
 
 

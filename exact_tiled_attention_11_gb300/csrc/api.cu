@@ -47,6 +47,21 @@ bool make_map_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, u
   return r == CUDA_SUCCESS;
 }
 
+// 3-D byte tensor [d2][d1][d0] (d0 contiguous, a multiple of 16 bytes) with a
+// box of (128, 128, 1) bytes and 128-byte swizzle: one e4m3 tile.
+bool make_map_u8(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {d0, std::max<uint64_t>(d1, 1), std::max<uint64_t>(d2, 1)};
+  cuuint64_t strides[2] = {d0, d0 * dims[1]};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -292,6 +307,82 @@ attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_p
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+int attn_fp8_padded_keys(int Nk) { return Nk < 0 ? -1 : (Nk + 15) / 16 * 16; }
+
+attn_status_t attn_fp8_quantize(const void *q, const void *k, const void *v, const float *signs, void *q8, void *k8,
+                                void *v8t, float *q_scale, float *k_scale, float *v_scale, int B, int H, int Hkv,
+                                int Nq, int Nk, int d, attn_stream_t stream) {
+  if (B < 0 || H < 0 || Hkv < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  const bool has_q = B > 0 && H > 0 && Nq > 0;
+  const bool has_kv = B > 0 && Hkv > 0 && Nk > 0;
+  if (has_q && (q == nullptr || q8 == nullptr || q_scale == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (has_kv && (k == nullptr || v == nullptr || k8 == nullptr || v8t == nullptr || k_scale == nullptr ||
+                 v_scale == nullptr))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q8) || !aligned16(k8) || !aligned16(v8t) ||
+      !aligned16(signs))
+    return ATTN_ERR_INVALID_ARG;
+  attn::Fp8QuantJob jq, jk, jv;
+  if (has_q) {
+    jq.x = static_cast<const uint16_t *>(q);
+    jq.out = static_cast<uint8_t *>(q8);
+    jq.scale = q_scale;
+    jq.planes = static_cast<long long>(B) * H;
+    jq.N = Nq;
+  }
+  if (has_kv) {
+    jk.x = static_cast<const uint16_t *>(k);
+    jk.out = static_cast<uint8_t *>(k8);
+    jk.scale = k_scale;
+    jk.planes = static_cast<long long>(B) * Hkv;
+    jk.N = Nk;
+    jv = jk;
+    jv.x = static_cast<const uint16_t *>(v);
+    jv.out = static_cast<uint8_t *>(v8t);
+    jv.scale = v_scale;
+    jv.n_pad = attn_fp8_padded_keys(Nk);
+  }
+  cudaError_t e = attn::launch_fp8_quantize(jq, jk, jv, signs, 1.0f / sqrtf(static_cast<float>(d)),
+                                            reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_fwd_fp8(const void *q8, const void *k8, const void *v8t, const float *q_scale,
+                           const float *k_scale, const float *v_scale, void *o, float *lse, int B, int H, int Hkv,
+                           int Nq, int Nk, int d, int causal, float scale, attn_stream_t stream) {
+  if (B < 0 || H < 0 || Hkv < 0 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || H == 0 || Nq == 0) return ATTN_OK;
+  if (Hkv == 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (q8 == nullptr || q_scale == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (Nk > 0 && (k8 == nullptr || v8t == nullptr || k_scale == nullptr || v_scale == nullptr))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8t) || !aligned16(o) || (lse && !aligned16(lse)))
+    return ATTN_ERR_INVALID_ARG;
+  attn::Fp8Maps maps;
+  // with Nk == 0 the K/V maps are never read; they only need a valid shape
+  const void *kb = Nk > 0 ? k8 : q8;
+  const void *vb = Nk > 0 ? v8t : q8;
+  if (!make_map_u8(&maps.q, q8, d, Nq, static_cast<uint64_t>(B) * H) ||
+      !make_map_u8(&maps.k, kb, d, Nk, static_cast<uint64_t>(B) * Hkv) ||
+      !make_map_u8(&maps.vt, vb, Nk > 0 ? attn_fp8_padded_keys(Nk) : 16, d, static_cast<uint64_t>(B) * Hkv))
+    return ATTN_ERR_CUDA;
+  PrefillOut out;
+  out.o = o;
+  out.lse = lse;
+  out.o_b = static_cast<long long>(H) * Nq * d;
+  out.o_h = static_cast<long long>(Nq) * d;
+  out.o_r = d;
+  out.l_b = static_cast<long long>(H) * Nq;
+  out.l_h = Nq;
+  out.l_r = 1;
+  cudaError_t e = attn::launch_prefill_fp8(maps, q_scale, k_scale, v_scale, out, B, H, Hkv, Nq, Nk, causal != 0,
+                                           scale, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 size_t attn_decode_workspace_size(int B, int H, int d, int max_splits) {
   if (B <= 0 || H <= 0 || d <= 0 || max_splits <= 0) return 0;
   return decode_ws_bytes(B, H, d, max_splits);
@@ -387,12 +478,13 @@ attn_status_t merge_partials(const float *m, const float *l, const float *o_tild
 attn_status_t attn_device_error(uint32_t *code, int clear) {
   if (code == nullptr) return ATTN_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
-  unsigned int a = 0, b = 0, c = 0;
+  unsigned int a = 0, b = 0, c = 0, f = 0;
   if (attn::device_error_decode(&a, clear != 0) != cudaSuccess ||
       attn::device_error_prefill_f32(&b, clear != 0) != cudaSuccess ||
-      attn::device_error_prefill_bf16(&c, clear != 0) != cudaSuccess)
+      attn::device_error_prefill_bf16(&c, clear != 0) != cudaSuccess ||
+      attn::device_error_prefill_fp8(&f, clear != 0) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  *code = a | b | c;
+  *code = a | b | c | f;
   return ATTN_OK;
 }
 

@@ -66,9 +66,37 @@ cudaError_t launch_prefill_bf16(const PrefillMaps &maps, const PrefillOut &out, 
                                 int Nk, int d, bool causal, float scale, cudaStream_t stream,
                                 const PrefillLayout &layout = PrefillLayout());
 
+// fp8_quantize.cu: one tensor of the FP8 inputs (d = 128).  x [planes, N, 128]
+// bf16 (raw bits); codes [planes, N, 128] e4m3, or, for V, transposed
+// [planes, 128, n_pad] (n_pad a multiple of 16, keys N .. n_pad-1 zero);
+// scale [planes, ceil(N / 128)] fp32.
+struct Fp8QuantJob {
+  const uint16_t *x = nullptr;
+  uint8_t *out = nullptr;
+  float *scale = nullptr;
+  long long planes = 0;
+  int N = 0;
+  int n_pad = 0;
+};
+// q and k are multiplied by diag(signs) H_128 first unless signs is null; their
+// stored scales then carry transform_norm (1 / sqrt(128)).  v is never transformed.
+cudaError_t launch_fp8_quantize(const Fp8QuantJob &q, const Fp8QuantJob &k, const Fp8QuantJob &v, const float *signs,
+                                float transform_norm, cudaStream_t stream);
+
+// prefill_fp8.cu: exact-attention forward over e4m3 blocks (d = 128): q8 [B, H, Nq, 128],
+// k8 [B, Hkv, Nk, 128] and v8t [B, Hkv, 128, Nk_pad] through 128 x 128-byte TMA boxes,
+// per-block scales as written by launch_fp8_quantize; O and LSE as PrefillOut.
+struct Fp8Maps {
+  CUtensorMap q, k, vt;
+};
+cudaError_t launch_prefill_fp8(const Fp8Maps &maps, const float *q_scale, const float *k_scale, const float *v_scale,
+                               const PrefillOut &out, int B, int H, int Hkv, int Nq, int Nk, bool causal, float scale,
+                               cudaStream_t stream);
+
 // Per-translation-unit device error words (see common.cuh).
 cudaError_t device_error_decode(unsigned int *value, bool clear);
 cudaError_t device_error_prefill_f32(unsigned int *value, bool clear);
 cudaError_t device_error_prefill_bf16(unsigned int *value, bool clear);
+cudaError_t device_error_prefill_fp8(unsigned int *value, bool clear);
 
 }  // namespace attn

@@ -148,6 +148,45 @@ attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_p
                              int max_pages_per_seq, int num_pages, int causal, float scale, attn_stream_t stream);
 
 /*
+ * FP8 attention: attn_fp8_quantize then attn_fwd_fp8.
+ *
+ * Follows "3.4 Attention Kernels", "FlashAttention-2 and -3": FlashAttention-3's
+ * FP8 attention, with block quantisation and "incoherent processing" (a random
+ * orthogonal transform against outliers).  Readings of that prose: the
+ * transform is M = diag(signs) H_d / sqrt(d) (H_d Sylvester's Hadamard matrix,
+ * signs a random +-1 vector) applied to Q and K, which leaves Q K^T unchanged;
+ * a block is one 128-row tile of one head, with one fp32 scale = amax / 448
+ * and e4m3 codes of x / scale (round to nearest even, saturating).  d = 128 only.
+ *
+ * attn_fp8_quantize -- quantise bf16 q [B, H, Nq, 128], k and v [B, Hkv, Nk, 128]:
+ *  signs     [128] fp32 +-1, device, 16-byte aligned; NULL = no transform
+ *  q8        [B, H, Nq, 128]        e4m3 codes of q M (written)
+ *  k8        [B, Hkv, Nk, 128]      e4m3 codes of k M (written)
+ *  v8t       [B, Hkv, 128, Nk_pad]  e4m3 codes of v, TRANSPOSED (keys contiguous),
+ *                                   Nk_pad = attn_fp8_padded_keys(Nk); keys Nk.. are 0
+ *  q_scale   [B, H, ceil(Nq / 128)]   fp32 block scales (dequantised x' = code * scale)
+ *  k_scale, v_scale [B, Hkv, ceil(Nk / 128)]
+ * All buffers are the caller's (nothing is allocated); one kernel launch.
+ */
+int attn_fp8_padded_keys(int Nk);
+attn_status_t attn_fp8_quantize(const void *q, const void *k, const void *v, const float *signs, void *q8,
+                                void *k8, void *v8t, float *q_scale, float *k_scale, float *v_scale, int B, int H,
+                                int Hkv, int Nq, int Nk, int d, attn_stream_t stream);
+
+/*
+ * attn_fwd_fp8 -- exact attention forward over the FP8 blocks written by
+ * attn_fp8_quantize: S = scale * (q8 k8^T) * sq * sk per block pair, the online
+ * softmax of attn_fwd (causal tile skipping, mask aligned to the last key when
+ * Nq != Nk, GQA), P rounded to e4m3 for P V (tcgen05 kind::f8f6f4 for both
+ * products).  o [B, H, Nq, 128] bf16, lse [B, H, Nq] fp32 (nullable).  The
+ * result equals attention of the dequantised blocks up to P's 8-bit rounding
+ * (|error| <= 2^-4 of the attended values' magnitude per key weight).
+ */
+attn_status_t attn_fwd_fp8(const void *q8, const void *k8, const void *v8t, const float *q_scale,
+                           const float *k_scale, const float *v_scale, void *o, float *lse, int B, int H, int Hkv,
+                           int Nq, int Nk, int d, int causal, float scale, attn_stream_t stream);
+
+/*
  * attn_decode_workspace_size -- bytes of device workspace attn_decode_paged
  * needs for up to max_splits partial results per (sequence, query head):
  * fp32 m and l [B, H, max_splits] and fp32 o~ [B, H, max_splits, d], each

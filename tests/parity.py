@@ -45,3 +45,49 @@ def check_lse(lse_gpu, lse_ref, what=""):
     mx = float(d.max()) if d.size else 0.0
     assert mx <= TOL_LSE, f"{what}: max |dLSE| = {mx:.3e} > {TOL_LSE}"
     return mx
+
+
+def fp8_tolerance(q_hat, k_hat, v_hat, v_scale, *, causal, scale, block=128):
+    """Per-element bound on |O_fp8 - O_oracle| for attention over dequantised FP8 blocks.
+
+    The FP8 kernel rounds p' = p * r_j to e4m3 before P V (r_j = v_scale_j /
+    max v_scale <= 1, p = 2^(s - m_ref) with the reference max m_ref within 8
+    (log2) of the row max, so l >= 1 * L where L = sum exp(S - S_max)).  e4m3
+    rounding moves x by at most max(2^-4 x, 2^-10), so key j moves the output
+    by at most b_j = max(2^-4 P_j, 2^-10 P_max / r_j) |v_j| (P the oracle's
+    softmax weights).  The errors of different keys are bounded, independent
+    roundings, so the bound is min(sum b_j, 7 sqrt(sum b_j^2)) (Hoeffding at
+    7 sigma), plus the bf16 rounding of O (2^-8 |O|), plus 1e-3 sum P_j |v_j|
+    for fp32 accumulation inside the tensor core.  Returns (O, LSE, tol)."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q_hat, k_hat, v_hat))
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    g = H // Hkv
+    O = np.zeros((B, H, Nq, d))
+    LSE = np.full((B, H, Nq), -np.inf)
+    tol = np.zeros((B, H, Nq, d))
+    vs = np.asarray(v_scale, dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            kv = h // g
+            S = scale * q[b, h] @ k[b, kv].T
+            if causal:
+                keep = np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq)
+                S = np.where(keep, S, -np.inf)
+            smax = S.max(axis=1, keepdims=True)
+            live = np.isfinite(smax[:, 0])
+            E = np.where(live[:, None], np.exp(S - np.where(live[:, None], smax, 0.0)), 0.0)
+            L = E.sum(axis=1, keepdims=True)
+            P = np.where(live[:, None], E / np.where(L > 0, L, 1.0), 0.0)
+            O[b, h] = P @ v[b, kv]
+            LSE[b, h] = np.where(live, smax[:, 0] + np.log(np.where(L[:, 0] > 0, L[:, 0], 1.0)), -np.inf)
+            vmax = vs[b, kv].max() if vs[b, kv].size else 0.0
+            r = np.where(vs[b, kv] > 0, np.maximum(vs[b, kv] / (vmax if vmax > 0 else 1.0), 2.0 ** -20), 1.0)
+            r_key = np.repeat(r, block)[:Nk]
+            pmax = P.max(axis=1, keepdims=True) if Nk else np.zeros((Nq, 1))
+            bj = np.maximum(2.0 ** -4 * P, 2.0 ** -10 * pmax / r_key[None, :]) * (P > 0)
+            av = np.abs(v[b, kv])
+            lin = bj @ av
+            quad = np.sqrt((bj ** 2) @ (av ** 2))
+            tol[b, h] = np.minimum(lin, 7 * quad) + 2.0 ** -8 * np.abs(O[b, h]) + 1e-3 * (P @ av) + 1e-6
+    return O, LSE, tol
