@@ -11,7 +11,12 @@
 // with the same block-wise online softmax, causal tile skipping, warp roles
 // and tensor-memory plan as the bf16 kernel (prefill_bf16.cu): one CTA per
 // pair of 128-row query tiles, a TMA warp for Q and K (3-stage ring), a TMA
-// warp for V, an MMA warp polling both chains, and two softmax warpgroups.
+// warp for V (2-stage ring), an MMA warp polling both chains, and two softmax
+// warpgroups.  The e4m3 tiles are half the bf16 size, which leaves room for two
+// P buffers per chain: softmax writes P(j) while P(j-1) V is still running and
+// waits for that product only when it must rescale o~ (the lazy rescale makes
+// that rare).  The MMA warp tests all of its pending conditions in one round
+// trip (one mbarrier test per lane, one ballot).
 //
 // V's per-block scale sv_j enters through P: softmax writes
 // p'_j = p * r_j with r_j = sv_j / max_i sv_i <= 1 (a shift of the exponent,
@@ -33,6 +38,8 @@ constexpr int BM = 128;      // query rows per tile (= TMEM lanes)
 constexpr int BN = 128;      // keys per K/V tile
 constexpr int D = 128;       // head dimension (one 128-byte e4m3 row)
 constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+constexpr int kPBufs = 2;                  // P buffers per chain
 constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -41,12 +48,13 @@ constexpr int kTileBytes = 128 * 128;      // 128 rows x 128 one-byte elements, 
 struct Fp8Smem {
   alignas(1024) uint8_t q[2][kTileBytes];
   alignas(1024) uint8_t k[kKStages][kTileBytes];
-  alignas(1024) uint8_t v[kTileBytes];     // V^T tile: 128 rows (d) x 128 keys
-  alignas(1024) uint8_t p[2][kTileBytes];  // P_A, P_B: 128 rows x 128 keys
+  alignas(1024) uint8_t v[kVStages][kTileBytes];    // V^T tiles: 128 rows (d) x 128 keys
+  alignas(1024) uint8_t p[2][kPBufs][kTileBytes];   // P of chains A and B: 128 rows x 128 keys
   uint64_t q_full;
   uint64_t k_full[kKStages], k_empty[kKStages];
-  uint64_t v_full, v_empty;
-  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full[2][kPBufs], pv_done[2][kPBufs];   // per P buffer, so phases never alias
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -197,13 +205,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.k_full[s]), 1);
       mbar_init(smem_u32(&sm.k_empty[s]), 1);
     }
-    mbar_init(smem_u32(&sm.v_full), 1);
-    mbar_init(smem_u32(&sm.v_empty), 1);
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(smem_u32(&sm.v_full[s]), 1);
+      mbar_init(smem_u32(&sm.v_empty[s]), 1);
+    }
     for (int c = 0; c < 2; ++c) {
       mbar_init(smem_u32(&sm.s_full[c]), 1);
       mbar_init(smem_u32(&sm.s_free[c]), 128);
-      mbar_init(smem_u32(&sm.p_full[c]), 128);
-      mbar_init(smem_u32(&sm.pv_done[c]), 1);
+      for (int pb = 0; pb < kPBufs; ++pb) {
+        mbar_init(smem_u32(&sm.p_full[c][pb]), 128);
+        mbar_init(smem_u32(&sm.pv_done[c][pb]), 1);
+      }
     }
     mbar_init(smem_u32(&sm.mma_done), 1);
     sm.abort = 0;
@@ -248,19 +260,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 2) {
-    // ================================================================ TMA: V^T (single stage)
+    // ================================================================ TMA: V^T (2-stage ring)
     if (lane == 0) {
       tma_prefetch_desc(&tm_vt);
       const uint64_t keep = l2_policy_evict_last();
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
-        if (j >= 1 && !mbar_wait(smem_u32(&sm.v_empty), (j - 1) & 1, &sm.abort)) break;
-        const uint32_t vbar = smem_u32(&sm.v_full);
+        const int vs = j % kVStages;
+        if (j >= kVStages && !mbar_wait(smem_u32(&sm.v_empty[vs]), ((j / kVStages) - 1) & 1, &sm.abort)) break;
+        const uint32_t vbar = smem_u32(&sm.v_full[vs]);
         mbar_arrive_expect_tx(vbar, kTileBytes);
-        tma_load_3d_hint(smem_u32(sm.v), &tm_vt, vbar, j * BN, 0, kv_plane, keep);
+        tma_load_3d_hint(smem_u32(sm.v[vs]), &tm_vt, vbar, j * BN, 0, kv_plane, keep);
         ++issued;
       }
-      if (issued > 0) mbar_wait(smem_u32(&sm.v_full), (issued - 1) & 1, nullptr);
+      for (int s = 0; s < kVStages && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / kVStages) * kVStages;
+        mbar_wait(smem_u32(&sm.v_full[s]), (last / kVStages) & 1, nullptr);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -273,30 +289,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc05::fence_after_sync();
     unsigned long long t_idle = 0;
     uint32_t spins = 0;
-    auto ready = [&](uint64_t *bar, uint32_t parity) -> bool {
-      return __shfl_sync(0xffffffffu, mbar_test(smem_u32(bar), parity) ? 1 : 0, 0) != 0;
-    };
     while (ok && (pv_next[0] < n_tiles[0] || pv_next[1] < n_tiles[1])) {
+      // Every condition of this pass in one round trip: lane 4c + 0 tests "S_c free",
+      // 4c + 1 "K ready for S_c", 4c + 2 "P_c written", 4c + 3 "V ready for P_c V".
+      const int cl = (lane >> 2) & 1;
+      const int jq_l = cl ? qk_next[1] : qk_next[0];
+      const int jp_l = cl ? pv_next[1] : pv_next[0];
+      bool r = true;
+      if (lane < 8) {
+        const int kind = lane & 3;
+        uint32_t bar, par;
+        if (kind == 0) {
+          bar = smem_u32(&sm.s_free[cl]);
+          par = (jq_l - 1) & 1;
+        } else if (kind == 1) {
+          bar = smem_u32(&sm.k_full[jq_l % kKStages]);
+          par = (jq_l / kKStages) & 1;
+        } else if (kind == 2) {
+          bar = smem_u32(&sm.p_full[cl][jp_l % kPBufs]);
+          par = (jp_l / kPBufs) & 1;
+        } else {
+          bar = smem_u32(&sm.v_full[jp_l % kVStages]);
+          par = (jp_l / kVStages) & 1;
+        }
+        r = (kind == 0 && jq_l == 0) || mbar_test(bar, par);
+      }
+      const uint32_t rdy = __ballot_sync(0xffffffffu, r);
       bool progressed = false;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
+        // S_c(j) = Q_c K_j^T, once softmax has taken S_c(j-1) out of tensor memory
         const int jq = qk_next[c];
-        if (jq < n_tiles[c] && (jq == 0 || ready(&sm.s_free[c], (jq - 1) & 1)) &&
-            ready(&sm.k_full[jq % kKStages], (jq / kKStages) & 1)) {
+        if (jq < n_tiles[c] && ((rdy >> (4 * c)) & 3u) == 3u) {
           tc05::fence_after_sync();
-          const uint32_t q_addr = smem_u32(sm.q[c]);
-          const uint32_t k_addr = smem_u32(sm.k[jq % kKStages]);
+          const uint64_t da = tc05::sdesc_sw128(smem_u32(sm.q[c]), 16, 1024);
+          const uint64_t db = tc05::sdesc_sw128(smem_u32(sm.k[jq % kKStages]), 16, 1024);
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < D / 32; ++kk) {  // K = 32 e4m3 elements (32 bytes) per MMA
-            const uint64_t da = tc05::sdesc_sw128(q_addr + kk * 32, 16, 1024);
-            const uint64_t db = tc05::sdesc_sw128(k_addr + kk * 32, 16, 1024);
-            if (elect_one()) mma_f8(tmem + c * BN, da, db, idesc, kk > 0);
-            __syncwarp();
+            for (int kk = 0; kk < D / 32; ++kk)  // K = 32 e4m3 elements (32 bytes, descriptor +2) per MMA
+              mma_f8(tmem + c * BN, da + 2 * kk, db + 2 * kk, idesc, kk > 0);
+            tc05::commit(smem_u32(&sm.s_full[c]));
           }
-          if (elect_one()) tc05::commit(smem_u32(&sm.s_full[c]));
           __syncwarp();
           qk_next[c] = jq + 1;
           progressed = true;
+          // hand back K stages whose every reader has been issued
           while (k_rel < n_kv && (qk_next[0] > k_rel || k_rel >= n_tiles[0]) &&
                  (qk_next[1] > k_rel || k_rel >= n_tiles[1])) {
             if (elect_one()) tc05::commit(smem_u32(&sm.k_empty[k_rel % kKStages]));
@@ -304,25 +341,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++k_rel;
           }
         }
+        // O_c += P_c(j) V_j, once softmax has written P_c(j) (so S_c(j) was issued) and V_j has landed
         const int jp = pv_next[c];
-        if (jp < qk_next[c] && ready(&sm.p_full[c], jp & 1) && ready(&sm.v_full, jp & 1)) {
+        if (jp < n_tiles[c] && ((rdy >> (4 * c + 2)) & 3u) == 3u) {
           tc05::fence_after_sync();
-          const uint32_t p_addr = smem_u32(sm.p[c]);
-          const uint32_t v_addr = smem_u32(sm.v);
+          const uint64_t da = tc05::sdesc_sw128(smem_u32(sm.p[c][jp % kPBufs]), 16, 1024);
+          const uint64_t db = tc05::sdesc_sw128(smem_u32(sm.v[jp % kVStages]), 16, 1024);
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < BN / 32; ++kk) {
-            const uint64_t da = tc05::sdesc_sw128(p_addr + kk * 32, 16, 1024);
-            const uint64_t db = tc05::sdesc_sw128(v_addr + kk * 32, 16, 1024);
-            if (elect_one()) mma_f8(tmem + 2 * BN + c * BN, da, db, idesc, (jp > 0) || (kk > 0));
-            __syncwarp();
+            for (int kk = 0; kk < BN / 32; ++kk)
+              mma_f8(tmem + 2 * BN + c * BN, da + 2 * kk, db + 2 * kk, idesc, (jp > 0) || (kk > 0));
+            tc05::commit(smem_u32(&sm.pv_done[c][jp % kPBufs]));
           }
-          if (elect_one()) tc05::commit(smem_u32(&sm.pv_done[c]));
           __syncwarp();
           pv_next[c] = jp + 1;
           progressed = true;
           while (v_rel < n_kv && (pv_next[0] > v_rel || v_rel >= n_tiles[0]) &&
                  (pv_next[1] > v_rel || v_rel >= n_tiles[1])) {
-            if (elect_one()) tc05::commit(smem_u32(&sm.v_empty));
+            if (elect_one()) tc05::commit(smem_u32(&sm.v_empty[v_rel % kVStages]));
             __syncwarp();
             ++v_rel;
           }
@@ -359,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_addr = tmem + lane_addr + c * BN;
     const uint32_t o_addr = tmem + lane_addr + 2 * BN + c * BN;
-    const uint32_t p_row = smem_u32(sm.p[c]) + row * 128;
+    const uint32_t p_row0 = smem_u32(sm.p[c][0]) + row * 128;  // this row of P buffer 0 (buffer 1 follows)
     const int lim = causal ? min(q_row + shift + 1, Nk) : Nk;
     const float *ks = k_scale + static_cast<long long>(kv_plane) * n_kt_all;
     const float *vs = v_scale + static_cast<long long>(kv_plane) * n_kt_all;
@@ -449,30 +485,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       f2_split(add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3])), sum_lo, sum_hi);
       l = l * corr + (sum_lo + sum_hi) / r_j;
 
-      if (j > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.pv_done[c]), (j - 1) & 1, &sm.abort))) {
+      // P buffer pb was last read by P(j-2) V_{j-2}; o~ is rescaled in place (when this
+      // warp's rows moved their reference) only once P(j-1) V_{j-1} has completed
+      const int pb = j % kPBufs;
+      if (j >= kPBufs &&
+          !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.pv_done[c][pb]), ((j / kPBufs) - 1) & 1, &sm.abort))) {
+        ok = false;
+        break;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, move)) {
+        const int jb = (j - 1) % kPBufs;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(smem_u32(&sm.pv_done[c][jb]), ((j - 1) / kPBufs) & 1, &sm.abort))) {
           ok = false;
           break;
         }
         tc05::fence_after_sync();
-        if (__any_sync(0xffffffffu, move)) {
 #pragma unroll
-          for (int q4 = 0; q4 < D / 32; ++q4) rescale_o_chunk(o_addr + q4 * 32, corr);
-        }
+        for (int q4 = 0; q4 < D / 32; ++q4) rescale_o_chunk(o_addr + q4 * 32, corr);
       }
       // P row -> shared memory: keys 16ch .. 16ch+15 at chunk ch, chunk index XOR (row mod 8)
+      const uint32_t p_row = p_row0 + pb * kTileBytes;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
         st_shared_v4(p_row + (((ch ^ row) & 7) << 4), pr[4 * ch], pr[4 * ch + 1], pr[4 * ch + 2], pr[4 * ch + 3]);
       fence_proxy_async_smem();
       tc05::tmem_wait_st();
       tc05::fence_before_sync();
-      mbar_arrive(smem_u32(&sm.p_full[c]));
+      mbar_arrive(smem_u32(&sm.p_full[c][pb]));
     }
 
     // ---- epilogue: O = o~ * max sv / l, LSE = m + ln l
     if (ok && n_c > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.pv_done[c]), (n_c - 1) & 1, &sm.abort));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.pv_done[c][(n_c - 1) % kPBufs]),
+                                             ((n_c - 1) / kPBufs) & 1, &sm.abort));
       if (ok) {
         tc05::fence_after_sync();
         const float inv = (l > 0.f) ? v_max / l : 0.f;
