@@ -147,6 +147,8 @@ def kernel_source_sha(files):
 KERNEL_SOURCES = {
     "prefill_bf16": ["prefill_bf16.cu", "tc05.cuh", "common.cuh"],
     "decode_split": ["decode.cu", "common.cuh"],
+    "prefill_fp8": ["prefill_fp8.cu", "tc05.cuh", "common.cuh"],
+    "fp8_quantize": ["fp8_quantize.cu", "common.cuh"],
 }
 
 
@@ -189,6 +191,61 @@ def decode_bytes(kv):
     B, H, d = kv.q.shape
     pages_used = int(((kv.kv_lens.to(torch.int64) + kv.page_size - 1) // kv.page_size).sum())
     return kv.kv_bytes() + kv.q.numel() * 2 + pages_used * 4 + B * 4 + B * H * d * 2 + B * H * 4
+
+
+# ------------------------------------------------------------------ the FP8 variant of the prefill
+
+def fp8_variant(dev, d, t_peak, hbm_peak, reps=10):
+    """attn_fp8_quantize + attn_fwd_fp8 on the benchmark's prefill inputs (B=1, H=32,
+    Hkv=8, N=8192, d=128, causal), timed apart from the step: each launch between
+    its own pair of CUDA events, with a 256 MiB write between launches so that no
+    input is served from L2.  The fp8 tensor peak is the measured bf16 peak times
+    the nominal fp8/bf16 ratio (2)."""
+    import torch
+    import exact_tiled_attention_11_gb300 as lib
+    from exact_tiled_attention_11_gb300 import workloads as W
+    stream = torch.cuda.current_stream(dev)
+    signs = W.fp8_signs(128).to(dev)
+    x = lib.attn_fp8_quantize(d["q"], d["k"], d["v"], signs)
+    o = torch.empty_like(d["o"])
+    lse = torch.empty_like(d["lse"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        tot = 0.0
+        for _ in range(reps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            tot += e0.elapsed_time(e1)
+        return tot / reps
+
+    q_ms = timed(lambda: lib.attn_fp8_quantize(d["q"], d["k"], d["v"], signs, x))
+    a_ms = timed(lambda: lib.attn_fwd_fp8(x, o, lse, causal=True, scale=W.C3.scale))
+    if lib.attn_device_error() != 0:
+        raise SystemExit("a kernel recorded a device error in the FP8 measurement")
+    flops = W.C3.flops(causal=True)
+    n_in = d["q"].numel() + d["k"].numel() + d["v"].numel()
+    q_bytes = n_in * 2 + n_in + 4 * (x.q_scale.numel() + x.k_scale.numel() + x.v_scale.numel())
+    tf = flops / (a_ms * 1e-3) / 1e12
+    gbs = q_bytes / (q_ms * 1e-3) / 1e9
+    fp8_peak = 2.0 * t_peak
+    return {
+        "attention": {"kernel": "prefill_fp8_kernel", "value": tf, "unit": "TFLOP/s", "ms_per_call": a_ms,
+                      "roofline": {"bound": "tensor", "achieved": tf, "peak": fp8_peak, "unit": "TFLOP/s",
+                                   "frac": tf / fp8_peak, "traffic": recorded_traffic("prefill_fp8"),
+                                   "peak_source": "2 x measured bf16_tflops (nominal fp8/bf16 ratio)"}},
+        "quantize": {"kernel": "fp8_quantize_kernel", "value": gbs, "unit": "GB/s", "ms_per_call": q_ms,
+                     "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                                  "frac": gbs / hbm_peak, "traffic": recorded_traffic("fp8_quantize"),
+                                  "algorithmic_bytes_per_launch": q_bytes}},
+        "l2": "256 MiB write between launches",
+    }
 
 
 # ------------------------------------------------------------------ launch overhead (eager vs CUDA graph)
@@ -486,6 +543,7 @@ def run_ours(args, rank, local_rank, world):
         "clocks": clocks,
     }
     line["launch_overhead"] = launch_overhead(dev)
+    line["fp8"] = fp8_variant(dev, d, t_peak, hbm_peak)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(host, kv)
     print(json.dumps(line), flush=True)
@@ -496,6 +554,7 @@ def run_profile_case(args):
     """One kernel family alone, for ncu: W warm-up launches then one more launch.
 
     prefill: the long causal workload (B=1, H=32, Hkv=8, N=8192, d=128).
+    fp8:     the same inputs through attn_fp8_quantize + attn_fwd_fp8.
     decode:  the paged decode workload restricted to its first --decode-batch
              sequences (same length distribution and page placement recipe).
     """
@@ -508,6 +567,12 @@ def run_profile_case(args):
         q, k, v = (t.to(dev) for t in W.prefill_inputs_for(W.C3))
         for _ in range(args.warmup + 1):
             lib.attn_fwd(q, k, v, causal=True, scale=W.C3.scale)
+    elif args.profile == "fp8":
+        q, k, v = (t.to(dev) for t in W.prefill_inputs_for(W.C3))
+        signs = W.fp8_signs(128).to(dev)
+        for _ in range(args.warmup + 1):
+            x = lib.attn_fp8_quantize(q, k, v, signs)
+            lib.attn_fwd_fp8(x, causal=True, scale=W.C3.scale)
     else:
         kv = W.decode_inputs_for(W.C4, B=args.decode_batch)
         t = [x.to(dev) for x in (kv.q, kv.k_pages, kv.v_pages, kv.page_table, kv.kv_lens)]
@@ -526,7 +591,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--profile", choices=["prefill", "decode", "fp8"], default=None,
                     help="run one kernel family alone (for ncu) instead of the benchmark")
     ap.add_argument("--decode-batch", type=int, default=16)
     args = ap.parse_args(argv)
