@@ -73,12 +73,12 @@ int device_sm_count() {
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
 // Split-KV plan from arguments only (no device-to-host copy): chunks of at
-// most 128 pages (2 MiB of K/V per CTA at d = 128, long enough to amortise a
-// CTA's set-up), more splits when that gives fewer than ~6 CTAs per SM with
-// every sequence as long as the longest, and chunks of at least 8 pages.
+// most 256 pages (2 MiB of one KV head's K and V at d = 128, long enough to
+// amortise a CTA's set-up), more splits when that gives fewer than ~6 CTAs per
+// SM with every sequence as long as the longest, and chunks of at least 8 pages.
 int auto_splits(int B, int Hkv, int max_pages, int num_sms) {
   const int want_ctas = 6 * std::max(num_sms, 1);
-  int s = ceil_div(max_pages, 128);
+  int s = ceil_div(max_pages, 256);
   s = std::max(s, ceil_div(want_ctas, static_cast<long long>(B) * Hkv));
   s = std::min(s, ceil_div(max_pages, 8));
   return std::max(s, 1);
@@ -191,7 +191,7 @@ attn_status_t decode_launch(const DecodePlan &plan, const void *q, const void *k
   // with no pages at all every sequence's own keys are empty: only the extra partial (if any) counts
   cudaError_t e = attn::launch_merge(ws_m, ws_l, ws_o, nullptr, kv_lens, page_size,
                                      plan.has_pages ? plan.chunk : 1 << 30, B, H, plan.splits, d, o, true, lse,
-                                     extra_o, extra_lse, st);
+                                     extra_o, extra_lse, st, plan.has_pages);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -368,6 +368,10 @@ __global__ void __launch_bounds__(256)
                  int chunk_pages, int B, int H, int S, OutT *__restrict__ o_out, float *__restrict__ lse_out,
                  const __nv_bfloat16 *__restrict__ extra_o, const float *__restrict__ extra_lse) {
   constexpr int E = D / 32;  // elements per lane
+  // Launched as a programmatic dependent of the split kernel in the decode path:
+  // wait here until that grid has finished and its partials are visible (a no-op
+  // for an ordinary launch).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp_global >= B * H) return;
@@ -480,24 +484,33 @@ cudaError_t launch_decode_split(const CUtensorMap &tm_k, const CUtensorMap &tm_v
 cudaError_t launch_merge(const float *m, const float *l, const float *o_tilde, const int32_t *num_parts,
                          const int32_t *kv_lens, int page_size, int chunk_pages, int B, int H, int S, int d, void *o,
                          bool out_bf16, float *lse, const void *extra_o, const float *extra_lse,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, bool after_split) {
   const int warps = B * H;
   const int threads = 256;
   const int blocks = (warps * 32 + threads - 1) / threads;
   if (blocks == 0) return cudaSuccess;
+  // Right after the split kernel the merge is launched as its programmatic
+  // dependent, so that its launch overlaps the split kernel's last CTAs.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_split ? 1 : 0;
 #define ATTN_MERGE_LAUNCH(DD, T)                                                                              \
-  merge_kernel<DD, T><<<blocks, threads, 0, stream>>>(m, l, o_tilde, num_parts, kv_lens, page_size, chunk_pages, \
-                                                      B, H, S, static_cast<T *>(o), lse,                          \
-                                                      static_cast<const __nv_bfloat16 *>(extra_o), extra_lse)
-  if (d == 128) {
-    if (out_bf16) ATTN_MERGE_LAUNCH(128, __nv_bfloat16);
-    else ATTN_MERGE_LAUNCH(128, float);
-  } else {
-    if (out_bf16) ATTN_MERGE_LAUNCH(64, __nv_bfloat16);
-    else ATTN_MERGE_LAUNCH(64, float);
-  }
+  cudaLaunchKernelEx(&cfg, merge_kernel<DD, T>, m, l, o_tilde, num_parts, kv_lens, page_size, chunk_pages, B, H, \
+                     S, static_cast<T *>(o), lse, static_cast<const __nv_bfloat16 *>(extra_o), extra_lse)
+  cudaError_t e;
+  if (d == 128)
+    e = out_bf16 ? ATTN_MERGE_LAUNCH(128, __nv_bfloat16) : ATTN_MERGE_LAUNCH(128, float);
+  else
+    e = out_bf16 ? ATTN_MERGE_LAUNCH(64, __nv_bfloat16) : ATTN_MERGE_LAUNCH(64, float);
 #undef ATTN_MERGE_LAUNCH
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace attn

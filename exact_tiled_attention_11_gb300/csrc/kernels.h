@@ -19,7 +19,7 @@ cudaError_t launch_decode_split(const CUtensorMap &tm_k, const CUtensorMap &tm_v
 cudaError_t launch_merge(const float *m, const float *l, const float *o_tilde, const int32_t *num_parts,
                          const int32_t *kv_lens, int page_size, int chunk_pages, int B, int H, int S, int d, void *o,
                          bool out_bf16, float *lse, const void *extra_o, const float *extra_lse,
-                         cudaStream_t stream);
+                         cudaStream_t stream, bool after_split = false);
 
 // Where the prefill kernels write O and the LSE: element strides of the batch,
 // head and query-row dimensions (d is contiguous).  The plain [B, H, Nq, d] /
