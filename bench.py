@@ -470,13 +470,14 @@ def run_ours(args, rank, local_rank, world):
         d2h = sum(t.numel() * t.element_size() for t in (out_o, out_lse, out_do, out_dlse))
         pre_h2d = sum(pin[n].numel() * pin[n].element_size() for n in ("q", "k", "v"))
 
+        bufs = (d["q"], d["k"], d["v"], d["o"], d["lse"])
+
         def e2e_step(evs):
             evs[0].record(stream)
-            for n, dst in (("q", "q"), ("k", "k"), ("v", "v")):
-                d[dst].copy_(pin[n], non_blocking=True)
-            prefill()
-            out_o.copy_(d["o"], non_blocking=True)
-            out_lse.copy_(d["lse"], non_blocking=True)
+            # prefill through the host-buffer entry point: Q, K, V in and O, LSE out,
+            # pipelined with the attention by groups of KV heads inside the call
+            lib.attn_fwd_host(pin["q"], pin["k"], pin["v"], out_o, out_lse, buffers=bufs, causal=True,
+                              scale=W.C3.scale, stream=stream)
             evs[1].record(stream)
             d["dq"].copy_(pin["dq"], non_blocking=True)
             d["page_table"].copy_(pin["page_table"], non_blocking=True)
@@ -502,7 +503,9 @@ def run_ours(args, rank, local_rank, world):
                "prefill_h2d_bytes_per_step": pre_h2d,
                "decode": {"value": world * dec_bytes * args.steps / (e_dec * 1e-3) / 1e9, "unit": "GB/s"},
                "ms_per_step": (e_pre + e_dec) / args.steps,
-               "note": "decode KV pool is device-resident cache state; per step only q, page table and kv_lens go H2D"}
+               "note": ("prefill through attn_fwd_host (host buffers; copies pipelined with the attention "
+                        "inside the call); decode KV pool is device-resident cache state, per step only q, "
+                        "page table and kv_lens go H2D")}
 
     if rank != 0:
         return 0

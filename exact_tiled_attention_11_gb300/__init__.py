@@ -21,6 +21,7 @@ from ._lib import (  # noqa: F401
     attn_fwd,
     attn_fwd_cross,
     attn_fwd_fp8,
+    attn_fwd_host,
     attn_fwd_paged,
     attn_fwd_varlen,
     attn_status_string,

@@ -50,6 +50,9 @@ def load_library() -> ctypes.CDLL:
         vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.attn_fwd.restype = i32
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp]
+        lib.attn_fwd_host.restype = i32
+        lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
+                                      vp, vp, vp]
         lib.attn_fwd_cross.restype = i32
         lib.attn_fwd_cross.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp]
         lib.attn_fwd_varlen.restype = i32
@@ -141,6 +144,57 @@ def attn_fwd(q, k, v, o=None, lse=None, *, causal=False, scale=None, stream=None
     dt = ATTN_BF16 if q.dtype == torch.bfloat16 else ATTN_F32
     _check("attn_fwd", lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d,
                                     1 if causal else 0, scale, dt, _stream(stream, q.device)))
+    return o, lse
+
+
+_COPY_STREAMS = {}
+
+
+def _copy_streams(device):
+    """Two side streams per device for attn_fwd_host's copies (created once)."""
+    key = torch.device(device).index
+    if key not in _COPY_STREAMS:
+        _COPY_STREAMS[key] = (torch.cuda.Stream(device=device), torch.cuda.Stream(device=device))
+    return _COPY_STREAMS[key]
+
+
+def attn_fwd_host(q, k, v, o=None, lse=None, *, device=None, buffers=None, causal=False, scale=None, stream=None,
+                  copy_streams=None):
+    """attn_fwd on host tensors (q [B, H, N, d], k, v [B, Hkv, N, d], bf16 or fp32, CPU,
+    contiguous; pinned for overlap).  The copies in and out are pipelined with the
+    attention inside the call.  ``buffers`` = (q_dev, k_dev, v_dev, o_dev, lse_dev) on the
+    device (allocated when not given).  Returns (o, lse) on the host; the results are
+    complete once ``stream`` (default: the current stream) has reached this point."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype or t.dim() != 4:
+            raise ValueError(f"{n} must be a contiguous 4-D host tensor of q's dtype")
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("attn_fwd_host takes bf16 or fp32 tensors")
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, N, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, N, d] matching q")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if o is None:
+        o = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    if lse is None:
+        lse = torch.empty(B, H, N, dtype=torch.float32, pin_memory=True)
+    if buffers is None:
+        buffers = (torch.empty(q.shape, dtype=q.dtype, device=dev), torch.empty(k.shape, dtype=q.dtype, device=dev),
+                   torch.empty(k.shape, dtype=q.dtype, device=dev), torch.empty(q.shape, dtype=q.dtype, device=dev),
+                   torch.empty(B, H, N, dtype=torch.float32, device=dev))
+    qd, kd, vd, od, ld = buffers
+    for t, n in ((qd, "q_dev"), (kd, "k_dev"), (vd, "v_dev"), (od, "o_dev")):
+        _need(t, n, q.dtype, 4)
+    _need(ld, "lse_dev", torch.float32, 3)
+    cin, cout = _copy_streams(dev) if copy_streams is None else copy_streams
+    scale = (1.0 / d ** 0.5) if scale is None else float(scale)
+    dt = ATTN_BF16 if q.dtype == torch.bfloat16 else ATTN_F32
+    _check("attn_fwd_host", lib.attn_fwd_host(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(qd), _ptr(kd), _ptr(vd), _ptr(od), _ptr(ld),
+        B, H, Hkv, N, d, 1 if causal else 0, scale, dt, _stream(stream, dev),
+        ctypes.c_void_p(cin.cuda_stream), ctypes.c_void_p(cout.cuda_stream)))
     return o, lse
 
 

@@ -16,6 +16,7 @@ using attn::PrefillMaps;
 using attn::PrefillOut;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }  // the LSE (scalar stores)
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -102,7 +103,7 @@ attn_status_t fwd_impl(const void *q, const void *k, const void *v, void *o, flo
   if (B == 0 || H == 0 || Nq == 0) return ATTN_OK;
   if (Hkv == 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (q == nullptr || o == nullptr || (Nk > 0 && (k == nullptr || v == nullptr))) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned4(lse)))
     return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -150,7 +151,7 @@ attn_status_t decode_check(const void *q, const void *k_pages, const void *v_pag
   if (B == 0 || H == 0) return ATTN_OK;
   if (Hkv == 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (q == nullptr || o == nullptr || kv_lens == nullptr || workspace == nullptr) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(o) || (lse && !aligned16(lse)) || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || (lse && !aligned4(lse)) || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
   if (d != 128 || page_size != 16 || H / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
   if (max_pages_per_seq > 0 && num_pages > 0) {
     if (k_pages == nullptr || v_pages == nullptr || page_table == nullptr) return ATTN_ERR_INVALID_ARG;
@@ -216,6 +217,88 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
   return fwd_impl(q, k, v, o, lse, B, H, Hkv, N, N, d, causal, scale, dtype, stream);
 }
 
+attn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void *v_host, void *o_host,
+                            float *lse_host, void *q_dev, void *k_dev, void *v_dev, void *o_dev, float *lse_dev,
+                            int B, int H, int Hkv, int N, int d, int causal, float scale, attn_dtype_t dtype,
+                            attn_stream_t stream, attn_stream_t copy_in, attn_stream_t copy_out) {
+  if (B < 0 || H < 0 || Hkv < 0 || N < 0) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_F32 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (copy_in == nullptr || copy_out == nullptr || stream == copy_in || stream == copy_out || copy_in == copy_out)
+    return ATTN_ERR_INVALID_ARG;
+  if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+  if (Hkv == 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (q_host == nullptr || k_host == nullptr || v_host == nullptr || o_host == nullptr || q_dev == nullptr ||
+      k_dev == nullptr || v_dev == nullptr || o_dev == nullptr || (lse_host != nullptr && lse_dev == nullptr))
+    return ATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !(scale < INFINITY)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t cin = reinterpret_cast<cudaStream_t>(copy_in);
+  cudaStream_t cout = reinterpret_cast<cudaStream_t>(copy_out);
+  const int g = H / Hkv;
+  const long long planes = static_cast<long long>(B) * Hkv;  // (batch, KV head) planes
+  const int groups = static_cast<int>(std::min<long long>(4, planes));
+  const size_t es = dtype == ATTN_BF16 ? 2 : 4;
+  const size_t kv_plane = static_cast<size_t>(N) * d * es;   // bytes of one K (or V) plane
+  const size_t q_plane = kv_plane * g;                       // bytes of the plane's g query heads
+  const size_t l_plane = static_cast<size_t>(N) * g * sizeof(float);
+
+  cudaEvent_t start, in_done[4], fwd_done[4], out_done;
+  bool created = true;
+  created &= cudaEventCreateWithFlags(&start, cudaEventDisableTiming) == cudaSuccess;
+  created &= cudaEventCreateWithFlags(&out_done, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; i < groups; ++i) {
+    created &= cudaEventCreateWithFlags(&in_done[i], cudaEventDisableTiming) == cudaSuccess;
+    created &= cudaEventCreateWithFlags(&fwd_done[i], cudaEventDisableTiming) == cudaSuccess;
+  }
+  if (!created) return ATTN_ERR_CUDA;
+  attn_status_t status = ATTN_OK;
+  auto check = [&](cudaError_t e) {
+    if (e != cudaSuccess && status == ATTN_OK) status = ATTN_ERR_CUDA;
+  };
+  // the copies may only touch the device buffers once earlier work on `stream` is done
+  check(cudaEventRecord(start, st));
+  check(cudaStreamWaitEvent(cin, start, 0));
+  check(cudaStreamWaitEvent(cout, start, 0));
+  auto bytes = [](const void *p, size_t off) { return static_cast<const char *>(p) + off; };
+  auto wbytes = [](void *p, size_t off) { return static_cast<char *>(p) + off; };
+  for (int i = 0; i < groups && status == ATTN_OK; ++i) {
+    const long long p0 = planes * i / groups, p1 = planes * (i + 1) / groups;
+    const size_t np = static_cast<size_t>(p1 - p0);
+    check(cudaMemcpyAsync(wbytes(q_dev, p0 * q_plane), bytes(q_host, p0 * q_plane), np * q_plane,
+                          cudaMemcpyHostToDevice, cin));
+    check(cudaMemcpyAsync(wbytes(k_dev, p0 * kv_plane), bytes(k_host, p0 * kv_plane), np * kv_plane,
+                          cudaMemcpyHostToDevice, cin));
+    check(cudaMemcpyAsync(wbytes(v_dev, p0 * kv_plane), bytes(v_host, p0 * kv_plane), np * kv_plane,
+                          cudaMemcpyHostToDevice, cin));
+    check(cudaEventRecord(in_done[i], cin));
+    check(cudaStreamWaitEvent(st, in_done[i], 0));
+    // the group as np batches of g query heads sharing one KV head
+    const attn_status_t s = fwd_impl(bytes(q_dev, p0 * q_plane), bytes(k_dev, p0 * kv_plane),
+                                     bytes(v_dev, p0 * kv_plane), wbytes(o_dev, p0 * q_plane),
+                                     lse_dev ? lse_dev + p0 * (l_plane / sizeof(float)) : nullptr,
+                                     static_cast<int>(np), g, 1, N, N, d, causal, scale, dtype, stream);
+    if (s != ATTN_OK) status = s;
+    check(cudaEventRecord(fwd_done[i], st));
+    check(cudaStreamWaitEvent(cout, fwd_done[i], 0));
+    check(cudaMemcpyAsync(wbytes(o_host, p0 * q_plane), bytes(o_dev, p0 * q_plane), np * q_plane,
+                          cudaMemcpyDeviceToHost, cout));
+    if (lse_host != nullptr)
+      check(cudaMemcpyAsync(lse_host + p0 * (l_plane / sizeof(float)), lse_dev + p0 * (l_plane / sizeof(float)),
+                            np * l_plane, cudaMemcpyDeviceToHost, cout));
+  }
+  // `stream` covers everything the call queued
+  check(cudaEventRecord(out_done, cout));
+  check(cudaStreamWaitEvent(st, out_done, 0));
+  cudaEventDestroy(start);
+  cudaEventDestroy(out_done);
+  for (int i = 0; i < groups; ++i) {
+    cudaEventDestroy(in_done[i]);
+    cudaEventDestroy(fwd_done[i]);
+  }
+  return status;
+}
+
 attn_status_t attn_fwd_cross(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Hkv,
                              int Nq, int Nk, int d, int causal, float scale, attn_dtype_t dtype, attn_stream_t stream) {
   return fwd_impl(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, causal, scale, dtype, stream);
@@ -231,7 +314,7 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
   if (Hkv == 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (q == nullptr || o == nullptr || qo_indptr == nullptr || kv_indptr == nullptr) return ATTN_ERR_INVALID_ARG;
   if (total_k > 0 && (k == nullptr || v == nullptr)) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned4(lse)))
     return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   PrefillMaps maps;
@@ -270,7 +353,7 @@ attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_p
   if (B == 0 || H == 0 || max_q_len == 0 || total_q == 0) return ATTN_OK;
   if (Hkv == 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (q == nullptr || o == nullptr || qo_indptr == nullptr || kv_lens == nullptr) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(o) || (lse && !aligned16(lse))) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || (lse && !aligned4(lse))) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (page_size != 16) return ATTN_ERR_UNSUPPORTED;
   const bool has_pages = max_pages_per_seq > 0 && num_pages > 0;
@@ -359,7 +442,7 @@ attn_status_t attn_fwd_fp8(const void *q8, const void *k8, const void *v8t, cons
   if (q8 == nullptr || q_scale == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
   if (Nk > 0 && (k8 == nullptr || v8t == nullptr || k_scale == nullptr || v_scale == nullptr))
     return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8t) || !aligned16(o) || (lse && !aligned16(lse)))
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8t) || !aligned16(o) || (lse && !aligned4(lse)))
     return ATTN_ERR_INVALID_ARG;
   attn::Fp8Maps maps;
   // with Nk == 0 the K/V maps are never read; they only need a valid shape
@@ -468,7 +551,7 @@ attn_status_t merge_partials(const float *m, const float *l, const float *o_tild
   if (o_dtype != ATTN_F32 && o_dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
   if (B == 0 || H == 0) return ATTN_OK;
   if (m == nullptr || l == nullptr || o_tilde == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(o_tilde) || !aligned16(o) || (lse && !aligned16(lse))) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(o_tilde) || !aligned16(o) || (lse && !aligned4(lse))) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   cudaError_t e = attn::launch_merge(m, l, o_tilde, num_parts, nullptr, 0, 1, B, H, S, d, o, o_dtype == ATTN_BF16,
                                      lse, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));

@@ -9,8 +9,9 @@
  * workspace) and keeps it alive until the launched work has finished.
  *
  * Common rules
- *  - Device pointers must be 16-byte aligned and tensors dense, last
- *    dimension contiguous, in the layouts stated per call.
+ *  - Device pointers must be 16-byte aligned (log-sum-exp outputs: 4-byte)
+ *    and tensors dense, last dimension contiguous, in the layouts stated per
+ *    call.
  *  - Argument errors are detected on the host and returned before anything
  *    is launched (ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
  *    ATTN_ERR_WORKSPACE).  A failed launch returns ATTN_ERR_CUDA.  Kernel
@@ -77,6 +78,37 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype_t;
 attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                        int B, int H, int Hkv, int N, int d, int causal, float scale,
                        attn_dtype_t dtype, attn_stream_t stream);
+
+/*
+ * attn_fwd_host -- attn_fwd on inputs and outputs in HOST memory: the call
+ * copies Q, K, V in, computes, and copies O (and the LSE) out, pipelined so
+ * that the copies overlap the attention (no counterpart on the pages; it is
+ * the end-to-end form of attn_fwd for callers whose tensors live on the host,
+ * e.g. offloaded activations on a Grace-Blackwell node).
+ *
+ * The (batch, KV head) planes are cut into up to four contiguous groups (a KV
+ * head and its g = H / Hkv query heads are contiguous in the layouts below).
+ * Group i: host-to-device copies of its Q, K, V rows on copy_in; attention of
+ * the group on `stream` once they have landed; device-to-host copies of its O
+ * and LSE rows on copy_out once that attention is done.  One cudaMemcpyAsync
+ * per contiguous range; no memory is allocated (up to ten CUDA events are
+ * created and released per call).
+ *
+ *  q_host, k_host, v_host, o_host, lse_host   host pointers, layouts and dtype as attn_fwd
+ *             (lse_host may be NULL); page-locked memory is needed for the copies to
+ *             overlap the computation, pageable memory still gives correct results
+ *  q_dev, k_dev, v_dev, o_dev, lse_dev          device buffers of the same sizes (the
+ *             caller's; lse_dev may be NULL only if lse_host is)
+ *  stream     the compute stream (NULL: the default stream); the call is ordered after the
+ *             work already queued on it, and everything the call does (copies included) is
+ *             complete once `stream` has reached the point of the call's return
+ *  copy_in, copy_out   two more streams, distinct from each other and from `stream`
+ * Errors: as attn_fwd; ATTN_ERR_INVALID_ARG also for NULL or coinciding copy streams.
+ */
+attn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void *v_host, void *o_host,
+                            float *lse_host, void *q_dev, void *k_dev, void *v_dev, void *o_dev, float *lse_dev,
+                            int B, int H, int Hkv, int N, int d, int causal, float scale, attn_dtype_t dtype,
+                            attn_stream_t stream, attn_stream_t copy_in, attn_stream_t copy_out);
 
 /*
  * attn_fwd_cross -- attn_fwd with Nq query rows against Nk keys (Nq may differ

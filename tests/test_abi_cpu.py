@@ -66,7 +66,7 @@ def test_attn_fwd_argument_checks(lib):
     assert fwd(lib, q=NULL) == INVALID
     assert fwd(lib, o=NULL) == INVALID
     assert fwd(lib, k=MIS) == INVALID
-    assert fwd(lib, lse=MIS) == INVALID
+    assert fwd(lib, lse=ctypes.c_void_p(0x10002)) == INVALID   # the LSE needs 4-byte alignment
     assert fwd(lib, H=6, Hkv=4) == INVALID
     assert fwd(lib, Hkv=0) == INVALID
     assert fwd(lib, N=-1) == INVALID
@@ -129,3 +129,22 @@ def test_merge_partials_argument_checks(lib):
 
 def test_device_error_rejects_null(lib):
     assert lib.attn_device_error(None, 0) == INVALID
+
+
+def test_fwd_host_rejects_bad_streams_before_any_work(lib):
+    """attn_fwd_host checks its streams and pointers on the host (no GPU needed)."""
+    vp = ctypes.c_void_p
+    buf = ctypes.create_string_buffer(64)
+    p = ctypes.cast(buf, vp)
+    s1, s2 = vp(0x1000), vp(0x2000)
+    args = lambda cin, cout: (p, p, p, p, None, p, p, p, p, None, 1, 1, 1, 1, 64, 0, ctypes.c_float(0.125), 1, None,
+                              cin, cout)
+    assert lib.attn_fwd_host(*args(None, s2)) == INVALID      # no copy-in stream
+    assert lib.attn_fwd_host(*args(s1, s1)) == INVALID        # copy streams coincide
+    assert lib.attn_fwd_host(*args(s1, None)) == INVALID
+    bad = list(args(s1, s2))
+    bad[0] = None                                              # no host q
+    assert lib.attn_fwd_host(*bad) == INVALID
+    zero = list(args(s1, s2))
+    zero[13] = 0                                               # N == 0: no-op
+    assert lib.attn_fwd_host(*zero) == 0
