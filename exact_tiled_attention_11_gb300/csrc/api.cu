@@ -217,6 +217,9 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
   return fwd_impl(q, k, v, o, lse, B, H, Hkv, N, N, d, causal, scale, dtype, stream);
 }
 
+// attn_fwd_host: groups of (batch, KV head) planes in flight at once
+constexpr int kHostGroups = 4;
+
 attn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void *v_host, void *o_host,
                             float *lse_host, void *q_dev, void *k_dev, void *v_dev, void *o_dev, float *lse_dev,
                             int B, int H, int Hkv, int N, int d, int causal, float scale, attn_dtype_t dtype,
@@ -237,13 +240,13 @@ attn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void *
   cudaStream_t cout = reinterpret_cast<cudaStream_t>(copy_out);
   const int g = H / Hkv;
   const long long planes = static_cast<long long>(B) * Hkv;  // (batch, KV head) planes
-  const int groups = static_cast<int>(std::min<long long>(4, planes));
+  const int groups = static_cast<int>(std::min<long long>(kHostGroups, planes));
   const size_t es = dtype == ATTN_BF16 ? 2 : 4;
   const size_t kv_plane = static_cast<size_t>(N) * d * es;   // bytes of one K (or V) plane
   const size_t q_plane = kv_plane * g;                       // bytes of the plane's g query heads
   const size_t l_plane = static_cast<size_t>(N) * g * sizeof(float);
 
-  cudaEvent_t start, in_done[4], fwd_done[4], out_done;
+  cudaEvent_t start, in_done[kHostGroups], fwd_done[kHostGroups], out_done;
   bool created = true;
   created &= cudaEventCreateWithFlags(&start, cudaEventDisableTiming) == cudaSuccess;
   created &= cudaEventCreateWithFlags(&out_done, cudaEventDisableTiming) == cudaSuccess;
