@@ -338,6 +338,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(vbar, Smem::kTileBytes);
         load_kv_tile(smem_u32(sm.v), &tm_v, vbar, j, keep, pages);
         ++issued;
+        // V has one stage, so each tile's copy waits for the previous tile's P V:
+        // start bringing the next tile into L2 now (dense and ragged layouts)
+        if (!kPagedK && j + 1 < n_kv) {
+#pragma unroll
+          for (int x = 0; x < D / 64; ++x) {
+            if (kRaggedK)
+              tma_prefetch_l2(&tm_v, x * 64, kv_plane, k_base + (j + 1) * BN);
+            else
+              tma_prefetch_l2(&tm_v, x * 64, (j + 1) * BN, kv_plane);
+          }
+        }
       }
       if (issued > 0) mbar_wait(smem_u32(&sm.v_full), (issued - 1) & 1, nullptr);
     }
