@@ -152,7 +152,7 @@ attn_status_t decode_check(const void *q, const void *k_pages, const void *v_pag
   if (Hkv == 0 || H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (q == nullptr || o == nullptr || kv_lens == nullptr || workspace == nullptr) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(o) || (lse && !aligned4(lse)) || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
-  if (d != 128 || page_size != 16 || H / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
+  if ((d != 64 && d != 128) || page_size != 16 || H / Hkv > 16) return ATTN_ERR_UNSUPPORTED;
   if (max_pages_per_seq > 0 && num_pages > 0) {
     if (k_pages == nullptr || v_pages == nullptr || page_table == nullptr) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(k_pages) || !aligned16(v_pages)) return ATTN_ERR_INVALID_ARG;
@@ -185,7 +185,7 @@ attn_status_t decode_launch(const DecodePlan &plan, const void *q, const void *k
     if (!make_map_3d(&tm_k, k_pages, d, page_size, rows, page_size) ||
         !make_map_3d(&tm_v, v_pages, d, page_size, rows, page_size))
       return ATTN_ERR_CUDA;
-    cudaError_t e = attn::launch_decode_split(tm_k, tm_v, q, page_table, kv_lens, ws_m, ws_l, ws_o, B, H, Hkv,
+    cudaError_t e = attn::launch_decode_split(tm_k, tm_v, q, page_table, kv_lens, ws_m, ws_l, ws_o, B, H, Hkv, d,
                                               max_pages_per_seq, num_pages, plan.chunk, plan.splits, scale, st);
     if (e != cudaSuccess) return ATTN_ERR_CUDA;
   }

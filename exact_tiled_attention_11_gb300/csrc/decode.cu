@@ -9,13 +9,13 @@
 // through the page table.
 //
 // Data movement: a single producer thread streams each page of the chunk
-// (K and V, 16 tokens x 128 dims bf16 each, 4 KiB + 4 KiB) into a ring of
+// (K and V, 16 tokens x d dims bf16 each: 4 KiB + 4 KiB at d = 128) into a ring of
 // shared-memory stages with TMA tensor loads (128-byte swizzle), completion
 // signalled on mbarriers.  Four consumer warps take pages round-robin, each
 // keeping its own online-softmax state; the four states are merged exactly in
 // shared memory at the end.  Per page a consumer warp does the two small
-// contractions S = Q K^T (16 heads-rows x 16 tokens x 128) and O += P V
-// (16 x 128 x 16 tokens) with warp-level bf16 tensor-core MMAs; the GQA
+// contractions S = Q K^T (16 heads-rows x 16 tokens x d) and O += P V
+// (16 x d x 16 tokens) with warp-level bf16 tensor-core MMAs; the GQA
 // group's g <= 16 query heads are the rows, so every K/V byte loaded is used
 // g times.  Only the running row max m, the partial row sums and the output
 // fragments live in registers.
@@ -26,26 +26,33 @@ namespace attn {
 
 namespace {
 
-constexpr int kD = 128;                 // head dimension
 constexpr int kPage = 16;               // tokens per page
 constexpr int kConsumerWarps = 4;
-constexpr int kStages = 8;              // pages in flight per CTA
-constexpr int kHalfBytes = kPage * 64 * 2;        // one 64-column half of a K or V page: 2 KiB
-constexpr int kPageBytes = 2 * kHalfBytes;        // 4 KiB
-constexpr int kStageBytes = 2 * kPageBytes;       // K page + V page: 8 KiB
+constexpr int kHalfBytes = kPage * 64 * 2;        // one 64-column block of a K or V page: 2 KiB
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
+// Sizes for head dimension D (64 or 128): a stage holds one page of K and one of V;
+// the ring keeps 64 KiB in flight per CTA whatever D is.
+template <int D>
+struct DecodeGeom {
+  static constexpr int kPageBytes = (D / 64) * kHalfBytes;  // 4 KiB at d = 128
+  static constexpr int kStageBytes = 2 * kPageBytes;        // K page + V page
+  static constexpr int kStages = (64 * 1024) / kStageBytes;  // 8 at d = 128, 16 at d = 64
+};
+
+template <int D>
 struct DecodeSmem {
-  alignas(1024) uint8_t stage[kStages][kStageBytes];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  using G = DecodeGeom<D>;
+  alignas(1024) uint8_t stage[G::kStages][G::kStageBytes];
+  uint64_t full[G::kStages];
+  uint64_t empty[G::kStages];
   float warp_m[kConsumerWarps][16];
   float warp_l[kConsumerWarps][16];
   int abort;
 };
 // The per-warp output fragments are merged through the (then idle) stage
-// buffers: 4 warps x 16 rows x 128 fp32 = 32 KiB <= the ring's 64 KiB.
-static_assert(kConsumerWarps * 16 * kD * 4 <= kStages * kStageBytes, "merge scratch must fit in the ring");
+// buffers: 4 warps x 16 rows x d fp32 (32 KiB at d = 128) <= the ring's 64 KiB.
+static_assert(kConsumerWarps * 16 * 128 * 4 <= 64 * 1024, "merge scratch must fit in the ring");
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -75,15 +82,20 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
 
 // Rows 0..7 of the MMA tile hold query heads 0..7 of the group, rows 8..15
 // heads 8..15; kHiRows says whether any head lands in rows 8..15 (g > 8).
-template <bool kHiRows>
+template <int D, bool kHiRows>
 __global__ void __launch_bounds__(kThreads)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const __nv_bfloat16 *__restrict__ q, const int32_t *__restrict__ page_table,
                         const int32_t *__restrict__ kv_lens, float *__restrict__ ws_m, float *__restrict__ ws_l,
                         float *__restrict__ ws_o, int H, int Hkv, int max_pages, int num_pages, int chunk_pages,
                         int S, float scale_log2) {
+  using G = DecodeGeom<D>;
+  constexpr int kStages = G::kStages;
+  constexpr int kPageBytes = G::kPageBytes;
+  constexpr int kStageBytes = G::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
-  DecodeSmem &sm = *reinterpret_cast<DecodeSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  DecodeSmem<D> &sm =
+      *reinterpret_cast<DecodeSmem<D> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
@@ -148,10 +160,11 @@ __global__ void __launch_bounds__(kThreads)
             const uint32_t bar = smem_u32(&sm.full[s]);
             const uint32_t dst = smem_u32(&sm.stage[s][0]);
             mbar_arrive_expect_tx(bar, kStageBytes);
-            tma_load_3d_hint(dst, &tm_k, bar, 0, 0, c2, policy);
-            tma_load_3d_hint(dst + kHalfBytes, &tm_k, bar, 64, 0, c2, policy);
-            tma_load_3d_hint(dst + kPageBytes, &tm_v, bar, 0, 0, c2, policy);
-            tma_load_3d_hint(dst + kPageBytes + kHalfBytes, &tm_v, bar, 64, 0, c2, policy);
+#pragma unroll
+            for (int x = 0; x < D / 64; ++x) {
+              tma_load_3d_hint(dst + x * kHalfBytes, &tm_k, bar, x * 64, 0, c2, policy);
+              tma_load_3d_hint(dst + kPageBytes + x * kHalfBytes, &tm_v, bar, x * 64, 0, c2, policy);
+            }
             ++issued;
           }
         }
@@ -176,16 +189,16 @@ __global__ void __launch_bounds__(kThreads)
     const int r0 = lane >> 2;           // MMA rows r0 and r0 + 8
     const int cpair = (lane & 3) * 2;   // column pair within an 8-wide n tile
     // Q fragments (A operand, rows = the group's query heads), loaded once.
-    uint32_t qa[8][4];
+    uint32_t qa[D / 16][4];
     {
       const int h_lo = kvh * g + r0;
       const int h_hi = kvh * g + r0 + 8;
       const bool v_lo = r0 < g;
       const bool v_hi = kHiRows && (r0 + 8 < g);
-      const uint32_t *q_lo = reinterpret_cast<const uint32_t *>(q + (static_cast<size_t>(b) * H + h_lo) * kD);
-      const uint32_t *q_hi = reinterpret_cast<const uint32_t *>(q + (static_cast<size_t>(b) * H + h_hi) * kD);
+      const uint32_t *q_lo = reinterpret_cast<const uint32_t *>(q + (static_cast<size_t>(b) * H + h_lo) * D);
+      const uint32_t *q_hi = reinterpret_cast<const uint32_t *>(q + (static_cast<size_t>(b) * H + h_hi) * D);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
+      for (int ks = 0; ks < D / 16; ++ks) {
         const int c = ks * 16 + cpair;
         qa[ks][0] = v_lo ? q_lo[c / 2] : 0u;
         qa[ks][1] = v_hi ? q_hi[c / 2] : 0u;
@@ -193,9 +206,9 @@ __global__ void __launch_bounds__(kThreads)
         qa[ks][3] = v_hi ? q_hi[(c + 8) / 2] : 0u;
       }
     }
-    float acc[16][4];
+    float acc[D / 8][4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int i = 0; i < D / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     float m_lo = -INFINITY, m_hi = -INFINITY;  // running max (log2 units) of rows r0, r0 + 8
     float l_lo = 0.f, l_hi = 0.f;              // this lane's share of the running sums
 
@@ -215,7 +228,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
+      for (int ks = 0; ks < D / 16; ++ks) {
         // matrices: (tok 0-7, d lo), (tok 0-7, d hi), (tok 8-15, d lo), (tok 8-15, d hi)
         const int tok = ((mi >> 1) << 3) + mr;
         const int col = ks * 16 + ((mi & 1) << 3);
@@ -256,7 +269,7 @@ __global__ void __launch_bounds__(kThreads)
         l_lo *= c_lo;
         l_hi *= c_hi;
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
+        for (int t = 0; t < D / 8; ++t) {
           acc[t][0] *= c_lo;
           acc[t][1] *= c_lo;
           acc[t][2] *= c_hi;
@@ -284,7 +297,7 @@ __global__ void __launch_bounds__(kThreads)
 
       // ---- O += P V over the 16 n tiles of the head dimension
 #pragma unroll
-      for (int dt = 0; dt < 16; dt += 2) {
+      for (int dt = 0; dt < D / 8; dt += 2) {
         // matrices: (tok 0-7, d dt), (tok 8-15, d dt), (tok 0-7, d dt+1), (tok 8-15, d dt+1)
         const int tok = ((mi & 1) << 3) + mr;
         const int col = (dt + (mi >> 1)) * 8;
@@ -312,15 +325,15 @@ __global__ void __launch_bounds__(kThreads)
     // Stash this warp's unnormalised output rows for the cross-warp merge.
     // The ring is reused as scratch: wait until every warp has finished reading it.
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-    float *scratch = reinterpret_cast<float *>(&sm.stage[0][0]) + warp * 16 * kD;
+    float *scratch = reinterpret_cast<float *>(&sm.stage[0][0]) + warp * 16 * D;
 #pragma unroll
-    for (int dt = 0; dt < 16; ++dt) {
+    for (int dt = 0; dt < D / 8; ++dt) {
       const int col = dt * 8 + cpair;
-      scratch[r0 * kD + col] = acc[dt][0];
-      scratch[r0 * kD + col + 1] = acc[dt][1];
+      scratch[r0 * D + col] = acc[dt][0];
+      scratch[r0 * D + col + 1] = acc[dt][1];
       if (kHiRows) {
-        scratch[(r0 + 8) * kD + col] = acc[dt][2];
-        scratch[(r0 + 8) * kD + col + 1] = acc[dt][3];
+        scratch[(r0 + 8) * D + col] = acc[dt][2];
+        scratch[(r0 + 8) * D + col + 1] = acc[dt][3];
       }
     }
   }
@@ -330,9 +343,9 @@ __global__ void __launch_bounds__(kThreads)
   // ---- merge the four warp states exactly and write this chunk's partial
   //      (m in natural-log units of the scaled scores, l, o~)
   const float *scratch = reinterpret_cast<const float *>(&sm.stage[0][0]);
-  for (int idx = threadIdx.x; idx < g * kD; idx += kThreads) {
-    const int r = idx / kD;
-    const int e = idx % kD;
+  for (int idx = threadIdx.x; idx < g * D; idx += kThreads) {
+    const int r = idx / D;
+    const int e = idx % D;
     float m = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) m = fmaxf(m, sm.warp_m[w][r]);
@@ -343,10 +356,10 @@ __global__ void __launch_bounds__(kThreads)
       if (mw == -INFINITY) continue;  // a warp that saw no page contributes nothing
       const float c = ex2_approx(mw - m);
       l += c * sm.warp_l[w][r];
-      o += c * scratch[(w * 16 + r) * kD + e];
+      o += c * scratch[(w * 16 + r) * D + e];
     }
     const size_t slot = (static_cast<size_t>(b) * H + kvh * g + r) * S + split;
-    ws_o[slot * kD + e] = o;
+    ws_o[slot * D + e] = o;
     if (e == 0) {
       ws_m[slot] = m * kLn2;
       ws_l[slot] = l;
@@ -451,34 +464,38 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-size_t decode_smem_bytes() { return sizeof(DecodeSmem) + 1024; }
+size_t decode_smem_bytes(int d) { return (d == 64 ? sizeof(DecodeSmem<64>) : sizeof(DecodeSmem<128>)) + 1024; }
 
 ATTN_DEFINE_ERROR_ACCESSOR(device_error_decode)
 
+namespace {
+template <int D, bool kHiRows>
+cudaError_t launch_split_d(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const void *q,
+                           const int32_t *page_table, const int32_t *kv_lens, float *ws_m, float *ws_l, float *ws_o,
+                           int B, int H, int Hkv, int max_pages, int num_pages, int chunk_pages, int S, float scale,
+                           cudaStream_t stream) {
+  const size_t smem = sizeof(DecodeSmem<D>) + 1024;
+  auto kern = decode_split_kernel<D, kHiRows>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(S, Hkv, B), kThreads, smem, stream>>>(tm_k, tm_v, static_cast<const __nv_bfloat16 *>(q), page_table,
+                                                    kv_lens, ws_m, ws_l, ws_o, H, Hkv, max_pages, num_pages,
+                                                    chunk_pages, S, scale * kLog2e);
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_decode_split(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const void *q,
                                 const int32_t *page_table, const int32_t *kv_lens, float *ws_m, float *ws_l,
-                                float *ws_o, int B, int H, int Hkv, int max_pages, int num_pages, int chunk_pages,
-                                int S, float scale, cudaStream_t stream) {
-  const int g = H / Hkv;
-  const size_t smem = decode_smem_bytes();
-  dim3 grid(S, Hkv, B);
-  const float scale_log2 = scale * kLog2e;
-  if (g > 8) {
-    auto kern = decode_split_kernel<true>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, stream>>>(tm_k, tm_v, static_cast<const __nv_bfloat16 *>(q), page_table, kv_lens,
-                                           ws_m, ws_l, ws_o, H, Hkv, max_pages, num_pages, chunk_pages, S,
-                                           scale_log2);
-  } else {
-    auto kern = decode_split_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, stream>>>(tm_k, tm_v, static_cast<const __nv_bfloat16 *>(q), page_table, kv_lens,
-                                           ws_m, ws_l, ws_o, H, Hkv, max_pages, num_pages, chunk_pages, S,
-                                           scale_log2);
-  }
-  return cudaGetLastError();
+                                float *ws_o, int B, int H, int Hkv, int d, int max_pages, int num_pages,
+                                int chunk_pages, int S, float scale, cudaStream_t stream) {
+  const bool hi = H / Hkv > 8;
+#define ATTN_SPLIT(DD, HI)                                                                                     \
+  launch_split_d<DD, HI>(tm_k, tm_v, q, page_table, kv_lens, ws_m, ws_l, ws_o, B, H, Hkv, max_pages, num_pages, \
+                         chunk_pages, S, scale, stream)
+  if (d == 64) return hi ? ATTN_SPLIT(64, true) : ATTN_SPLIT(64, false);
+  return hi ? ATTN_SPLIT(128, true) : ATTN_SPLIT(128, false);
+#undef ATTN_SPLIT
 }
 
 cudaError_t launch_merge(const float *m, const float *l, const float *o_tilde, const int32_t *num_parts,

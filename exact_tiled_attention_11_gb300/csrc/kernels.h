@@ -8,12 +8,12 @@
 
 namespace attn {
 
-// decode.cu
-size_t decode_smem_bytes();
+// decode.cu (d = 64 or 128)
+size_t decode_smem_bytes(int d);
 cudaError_t launch_decode_split(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const void *q,
                                 const int32_t *page_table, const int32_t *kv_lens, float *ws_m, float *ws_l,
-                                float *ws_o, int B, int H, int Hkv, int max_pages, int num_pages, int chunk_pages,
-                                int S, float scale, cudaStream_t stream);
+                                float *ws_o, int B, int H, int Hkv, int d, int max_pages, int num_pages,
+                                int chunk_pages, int S, float scale, cudaStream_t stream);
 // extra_o / extra_lse (nullable): one more partial per (sequence, head), given as a
 // normalised output O [B, H, d] bf16 with its LSE [B, H], i.e. (m, l, o~) = (LSE, 1, O).
 cudaError_t launch_merge(const float *m, const float *l, const float *o_tilde, const int32_t *num_parts,

@@ -255,7 +255,7 @@ size_t attn_decode_workspace_size(int B, int H, int d, int max_splits);
  *              ceil(pages_b / chunk) partials.  No device-to-host copy is made.
  *  workspace   >= attn_decode_workspace_size(B, H, d, num_splits used) bytes;
  *              with num_splits <= 0 pass the size for attn_decode_max_splits().
- *  Supported: d == 128, page_size == 16, H / Hkv <= 16.  Results are
+ *  Supported: d in {64, 128}, page_size == 16, H / Hkv <= 16.  Results are
  *  deterministic for a given num_splits.
  */
 attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,

@@ -98,7 +98,7 @@ def test_attn_decode_paged_argument_checks(lib):
     assert dec(lib, vp=MIS) == INVALID
     assert dec(lib, H=30, Hkv=8) == INVALID
     assert dec(lib, scale=0.0) == INVALID
-    assert dec(lib, d=64) == UNSUPPORTED
+    assert dec(lib, d=96) == UNSUPPORTED
     assert dec(lib, ps=32) == UNSUPPORTED
     assert dec(lib, H=64, Hkv=2) == UNSUPPORTED     # group of 32 query heads per KV head
     need = lib.attn_decode_workspace_size(2, 32, 128, 2)

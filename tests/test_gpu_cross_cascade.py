@@ -118,3 +118,20 @@ def test_cascade_matches_decode_when_prefix_is_in_the_pages(cuda):
     torch.cuda.synchronize()
     check_o(o_c.cpu(), o_d.cpu(), torch.bfloat16, "cascade vs paged")
     check_lse(lse_c.cpu(), lse_d.cpu(), "cascade vs paged")
+
+
+@pytest.mark.parametrize("Lp", [0, 300])
+def test_cascade_decode_head_dim_64(cuda, Lp):
+    lens = [0, 1, 16, 700]
+    kv = W.decode_inputs(len(lens), 16, 4, 64, 16, 1, 1, seed=Lp + 3, kv_lens=lens)
+    g = torch.Generator().manual_seed(Lp + 4)
+    pk = torch.randn(4, Lp, 64, generator=g).to(torch.bfloat16)
+    pv = torch.randn(4, Lp, 64, generator=g).to(torch.bfloat16)
+    t = [x.to(cuda) for x in (kv.q, kv.k_pages, kv.v_pages, kv.page_table, kv.kv_lens)]
+    o, lse = attn_cascade_decode(t[0], pk.to(cuda), pv.to(cuda), *t[1:])
+    torch.cuda.synchronize()
+    O, L = oracle.cascade_decode(kv.q, pk, pv, kv.k_pages, kv.v_pages, kv.page_table, kv.kv_lens,
+                                 scale=1 / math.sqrt(64))
+    check_o(o.cpu(), O, torch.bfloat16, f"cascade d=64 Lp={Lp}")
+    check_lse(lse.cpu(), L, f"cascade d=64 Lp={Lp}")
+    assert attn_device_error() == 0

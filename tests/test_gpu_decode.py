@@ -106,3 +106,15 @@ def test_c4_full_size_sampled(cuda):
     check_o(o[seqs], O[seqs], torch.bfloat16, "C4")
     check_lse(lse[seqs], L[seqs], "C4")
     assert attn_device_error(clear=False) == 0
+
+
+@pytest.mark.parametrize("num_splits", [0, 1, 4, 33])
+@pytest.mark.parametrize("H,Hkv", [(8, 8), (32, 8), (64, 4)])
+def test_head_dim_64(cuda, H, Hkv, num_splits):
+    """d = 64: one 64-column block per page, a 16-stage ring (the same bytes in flight)."""
+    kv = W.decode_inputs(6, H, Hkv, 64, 16, 1, 1, seed=H * 3 + Hkv, kv_lens=[1, 16, 17, 300, 2049, 0])
+    o, lse = run(kv, cuda, num_splits)
+    O, L = ref(kv)
+    check_o(o, O, torch.bfloat16, f"d=64 g={H // Hkv} splits={num_splits}")
+    check_lse(lse, L, f"d=64 g={H // Hkv} splits={num_splits}")
+    assert attn_device_error() == 0
