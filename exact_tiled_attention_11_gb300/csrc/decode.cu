@@ -97,9 +97,12 @@ __global__ void __launch_bounds__(kThreads)
   DecodeSmem<D> &sm =
       *reinterpret_cast<DecodeSmem<D> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  const int split = blockIdx.x;
-  const int kvh = blockIdx.y;
-  const int b = blockIdx.z;
+  // the grid is (KV head, sequence, split) with the split slowest: CTAs are dispatched
+  // chunk 0 of every sequence first, and the last ones dispatched are the final
+  // chunks of the longest sequences
+  const int split = blockIdx.z;
+  const int kvh = blockIdx.x;
+  const int b = blockIdx.y;
   const int g = H / Hkv;
   int L = kv_lens[b];
   if (L < 0 || L > max_pages * kPage) {
@@ -478,7 +481,7 @@ cudaError_t launch_split_d(const CUtensorMap &tm_k, const CUtensorMap &tm_v, con
   auto kern = decode_split_kernel<D, kHiRows>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<dim3(S, Hkv, B), kThreads, smem, stream>>>(tm_k, tm_v, static_cast<const __nv_bfloat16 *>(q), page_table,
+  kern<<<dim3(Hkv, B, S), kThreads, smem, stream>>>(tm_k, tm_v, static_cast<const __nv_bfloat16 *>(q), page_table,
                                                     kv_lens, ws_m, ws_l, ws_o, H, Hkv, max_pages, num_pages,
                                                     chunk_pages, S, scale * kLog2e);
   return cudaGetLastError();
