@@ -47,6 +47,39 @@ def check_lse(lse_gpu, lse_ref, what=""):
     return mx
 
 
+def fp8_tolerance_rows(q_rows, k, v, v_scale, rows, Nq, *, causal, scale, block=128):
+    """fp8_tolerance for selected query rows of one head: q_rows [len(rows), d] (the
+    dequantised query rows), k, v [Nk, d] (the head's dequantised keys and values),
+    v_scale [ceil(Nk / block)], rows their indices among Nq query rows."""
+    q = np.asarray(q_rows, dtype=np.float64)
+    kk = np.asarray(k, dtype=np.float64)
+    vv = np.asarray(v, dtype=np.float64)
+    Nk = kk.shape[0]
+    rows = np.asarray(rows, dtype=np.int64)
+    S = scale * q @ kk.T
+    if causal:
+        keep = np.arange(Nk)[None, :] <= rows[:, None] + (Nk - Nq)
+        S = np.where(keep, S, -np.inf)
+    smax = S.max(axis=1, keepdims=True) if Nk else np.full((len(rows), 1), -np.inf)
+    live = np.isfinite(smax[:, 0])
+    E = np.where(live[:, None], np.exp(S - np.where(live[:, None], smax, 0.0)), 0.0)
+    L = E.sum(axis=1, keepdims=True)
+    P = np.where(live[:, None], E / np.where(L > 0, L, 1.0), 0.0)
+    O = P @ vv
+    LSE = np.where(live, smax[:, 0] + np.log(np.where(L[:, 0] > 0, L[:, 0], 1.0)), -np.inf)
+    vs = np.asarray(v_scale, dtype=np.float64)
+    vmax = vs.max() if vs.size else 0.0
+    r = np.where(vs > 0, np.maximum(vs / (vmax if vmax > 0 else 1.0), 2.0 ** -20), 1.0)
+    r_key = np.repeat(r, block)[:Nk]
+    pmax = P.max(axis=1, keepdims=True) if Nk else np.zeros((len(rows), 1))
+    bj = np.maximum(2.0 ** -4 * P, 2.0 ** -10 * pmax / r_key[None, :]) * (P > 0)
+    av = np.abs(vv)
+    lin = bj @ av
+    quad = np.sqrt((bj ** 2) @ (av ** 2))
+    tol = np.minimum(lin, 7 * quad) + 2.0 ** -8 * np.abs(O) + 1e-3 * (P @ av) + 1e-6
+    return O, LSE, tol
+
+
 def fp8_tolerance(q_hat, k_hat, v_hat, v_scale, *, causal, scale, block=128):
     """Per-element bound on |O_fp8 - O_oracle| for attention over dequantised FP8 blocks.
 
@@ -61,33 +94,16 @@ def fp8_tolerance(q_hat, k_hat, v_hat, v_scale, *, causal, scale, block=128):
     for fp32 accumulation inside the tensor core.  Returns (O, LSE, tol)."""
     q, k, v = (np.asarray(x, dtype=np.float64) for x in (q_hat, k_hat, v_hat))
     B, H, Nq, d = q.shape
-    Hkv, Nk = k.shape[1], k.shape[2]
+    Hkv = k.shape[1]
     g = H // Hkv
     O = np.zeros((B, H, Nq, d))
     LSE = np.full((B, H, Nq), -np.inf)
     tol = np.zeros((B, H, Nq, d))
     vs = np.asarray(v_scale, dtype=np.float64)
+    rows = np.arange(Nq)
     for b in range(B):
         for h in range(H):
             kv = h // g
-            S = scale * q[b, h] @ k[b, kv].T
-            if causal:
-                keep = np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq)
-                S = np.where(keep, S, -np.inf)
-            smax = S.max(axis=1, keepdims=True)
-            live = np.isfinite(smax[:, 0])
-            E = np.where(live[:, None], np.exp(S - np.where(live[:, None], smax, 0.0)), 0.0)
-            L = E.sum(axis=1, keepdims=True)
-            P = np.where(live[:, None], E / np.where(L > 0, L, 1.0), 0.0)
-            O[b, h] = P @ v[b, kv]
-            LSE[b, h] = np.where(live, smax[:, 0] + np.log(np.where(L[:, 0] > 0, L[:, 0], 1.0)), -np.inf)
-            vmax = vs[b, kv].max() if vs[b, kv].size else 0.0
-            r = np.where(vs[b, kv] > 0, np.maximum(vs[b, kv] / (vmax if vmax > 0 else 1.0), 2.0 ** -20), 1.0)
-            r_key = np.repeat(r, block)[:Nk]
-            pmax = P.max(axis=1, keepdims=True) if Nk else np.zeros((Nq, 1))
-            bj = np.maximum(2.0 ** -4 * P, 2.0 ** -10 * pmax / r_key[None, :]) * (P > 0)
-            av = np.abs(v[b, kv])
-            lin = bj @ av
-            quad = np.sqrt((bj ** 2) @ (av ** 2))
-            tol[b, h] = np.minimum(lin, 7 * quad) + 2.0 ** -8 * np.abs(O[b, h]) + 1e-3 * (P @ av) + 1e-6
+            O[b, h], LSE[b, h], tol[b, h] = fp8_tolerance_rows(q[b, h], k[b, kv], v[b, kv], vs[b, kv], rows, Nq,
+                                                               causal=causal, scale=scale, block=block)
     return O, LSE, tol

@@ -23,7 +23,7 @@ from oracle import fp8 as F
 from exact_tiled_attention_11_gb300 import (Fp8Inputs, attn_device_error, attn_fp8_padded_keys, attn_fp8_quantize,
                                             attn_fwd_fp8)
 from exact_tiled_attention_11_gb300 import workloads as W
-from tests.parity import check_lse, f64, fp8_tolerance
+from tests.parity import check_lse, f64, fp8_tolerance, fp8_tolerance_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -162,3 +162,54 @@ def test_fp8_path_end_to_end_and_transform_benefit(cuda):
     # P's rounding adds little to the input quantisation's error, and the transform helps
     assert errs[True] < 1.25 * quant_only[True] and errs[False] < 1.25 * quant_only[False], (errs, quant_only)
     assert errs[True] < 0.6 * errs[False], errs
+
+
+def test_fp8_full_size_sampled(cuda):
+    """The benchmark's prefill inputs (B=1, H=32, Hkv=8, N=8192, d=128, causal) through the
+    FP8 path: the GPU quantiser on sampled blocks against the float64 quantiser, and the
+    FP8 attention of the oracle's blocks on sampled rows against the bound of P's rounding."""
+    cfg = W.C3
+    q, k, v = W.prefill_inputs_for(cfg)
+    signs = W.fp8_signs(128)
+    x = attn_fp8_quantize(q.to(cuda), k.to(cuda), v.to(cuda), signs.to(cuda))
+    torch.cuda.synchronize()
+    M = F.incoherent_transform(signs.numpy())
+    for name, t, codes, scales, transformed in (("q", q, x.q8, x.q_scale, True), ("k", k, x.k8, x.k_scale, True),
+                                               ("v", v, None, x.v_scale, False)):
+        for (h, blk) in ((0, 0), (3, 17), (7, 63), (1, 40)):
+            h = h % t.shape[1]
+            xs = f64(t[0, h, blk * 128:(blk + 1) * 128])
+            xs = xs @ M if transformed else xs
+            c_ref, s_ref, _ = F.quantize_blocks(xs[None, None])
+            np.testing.assert_allclose(float(scales[0, h, blk]), s_ref[0, 0, 0], rtol=1e-5, err_msg=f"{name} {h} {blk}")
+            r = xs / s_ref[0, 0, 0]
+            l1 = np.abs(f64(t[0, h, blk * 128:(blk + 1) * 128])).sum(axis=-1, keepdims=True) / math.sqrt(128)
+            delta = np.abs(r) * 1e-5 + (8 * 2.0 ** -24 * l1 / s_ref[0, 0, 0] if transformed else 0.0) + 1e-12
+            if codes is None:
+                got = x.v8t[0, h, :, blk * 128:(blk + 1) * 128].cpu().numpy().T
+            else:
+                got = codes[0, h, blk * 128:(blk + 1) * 128].cpu().numpy()
+            _check_codes(got, r, delta, f"{name} head {h} block {blk}")
+    # attention over the oracle's blocks: the sampled heads (and their KV heads) carry the
+    # oracle's codes, every other head all-zero blocks (valid input, outputs not checked),
+    # so the launch keeps the full shape
+    heads, kvs = [0, 5, 31], [0, 1, 7]
+    sub = _stored_scales(F.fp8_quantize(q[:, heads], k[:, kvs], v[:, kvs], signs.numpy()))
+    full = {"q8": np.zeros((1, 32, cfg.N, 128), np.uint8), "k8": np.zeros((1, 8, cfg.N, 128), np.uint8),
+            "v8": np.zeros((1, 8, cfg.N, 128), np.uint8), "q_scale": np.zeros((1, 32, cfg.N // 128)),
+            "k_scale": np.zeros((1, 8, cfg.N // 128)), "v_scale": np.zeros((1, 8, cfg.N // 128))}
+    for dst, src, idx in (("q", "q", heads), ("k", "k", kvs), ("v", "v", kvs)):
+        full[dst + "8"][:, idx] = sub[src + "8"]
+        full[dst + "_scale"][:, idx] = sub[src + "_scale"]
+    o, lse = attn_fwd_fp8(_upload(full, cuda), causal=True)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o.float()).all()
+    rng = np.random.default_rng(0)
+    for i, h in enumerate(heads):
+        rows = np.unique(np.concatenate([[0, 1, 127, 128, 8191], rng.integers(0, cfg.N, 60)]))
+        O, L, tol = fp8_tolerance_rows(sub["q_hat"][0, i][rows], sub["k_hat"][0, i], sub["v_hat"][0, i],
+                                       sub["v_scale"][0, i], rows, cfg.N, causal=True, scale=cfg.scale)
+        err = np.abs(f64(o[0, h, rows]) - O)
+        assert (err <= tol).all(), f"head {h}: max |dO| / bound = {float((err / tol).max()):.3f}"
+        check_lse(lse[0, h, rows].cpu(), L, f"fp8 full size head {h}")
+    assert attn_device_error() == 0
