@@ -449,41 +449,59 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e)
             if (kv0 + q4 * 32 + e >= lim) sr[q4][e] = __float_as_uint(-INFINITY);
       }
-      float mq[4];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float m = __uint_as_float(sr[q4][0]);
-#pragma unroll
-        for (int e = 1; e < 31; e += 2) m = max3(m, __uint_as_float(sr[q4][e]), __uint_as_float(sr[q4][e + 1]));
-        mq[q4] = fmaxf(m, __uint_as_float(sr[q4][31]));
-      }
-      const float m_new = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * c_j;
-      const bool move = m_new > m_ref + kRescaleThreshold;
-      const float m_next = move ? m_new : m_ref;
-      const float corr = (m_next == m_ref) ? 1.f : ex2_approx(m_ref - m_next);
-      m_ref = m_next;
-
-      // p' = 2^(acc * c_j - m_ref + log2 r_j), summed in eight partial sums, packed to e4m3
-      const float neg_m = ((m_ref == -INFINITY) ? 0.f : -m_ref) + log2_r;
-      const uint64_t negm2 = f2(neg_m, neg_m);
+      // p' = 2^(acc * c_j - m_ref + log2 r_j), summed, packed to e4m3.  First relative to the
+      // current reference without a row maximum: if the row sum of p stays <= 2^8, every p
+      // does, so the row maximum has not outgrown the reference by more than 2^8 and the
+      // reference stays.  Otherwise (and on a row's first scores) the maximum decides.
       const uint64_t c2 = f2(c_j, c_j);
-      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pr[32];
+      float sum = 0.f;
+      auto exp_pass = [&](float neg_m_ref) {
+        const uint64_t negm2 = f2(neg_m_ref + log2_r, neg_m_ref + log2_r);
+        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < 4; ++q4) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          float x0, x1, x2, x3;
-          f2_split(fma2(f2(__uint_as_float(sr[q4][e]), __uint_as_float(sr[q4][e + 1])), c2, negm2), x0, x1);
-          f2_split(fma2(f2(__uint_as_float(sr[q4][e + 2]), __uint_as_float(sr[q4][e + 3])), c2, negm2), x2, x3);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-          acc2[(e >> 2) & 3] = add2(acc2[(e >> 2) & 3], add2(f2(p0, p1), f2(p2, p3)));
-          pr[q4 * 8 + (e >> 2)] = pack_e4m3x4(p0, p1, p2, p3);
+          for (int e = 0; e < 32; e += 4) {
+            float x0, x1, x2, x3;
+            f2_split(fma2(f2(__uint_as_float(sr[q4][e]), __uint_as_float(sr[q4][e + 1])), c2, negm2), x0, x1);
+            f2_split(fma2(f2(__uint_as_float(sr[q4][e + 2]), __uint_as_float(sr[q4][e + 3])), c2, negm2), x2, x3);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+            acc2[(e >> 2) & 3] = add2(acc2[(e >> 2) & 3], add2(f2(p0, p1), f2(p2, p3)));
+            pr[q4 * 8 + (e >> 2)] = pack_e4m3x4(p0, p1, p2, p3);
+          }
+        }
+        float lo, hi;
+        f2_split(add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3])), lo, hi);
+        sum = lo + hi;
+      };
+      bool need_max = m_ref == -INFINITY;
+      if (!need_max) {
+        exp_pass(-m_ref);
+        need_max = sum > 256.f * r_j;
+      }
+      bool move = false;
+      float corr = 1.f;
+      if (need_max) {
+        float mq[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float m = __uint_as_float(sr[q4][0]);
+#pragma unroll
+          for (int e = 1; e < 31; e += 2) m = max3(m, __uint_as_float(sr[q4][e]), __uint_as_float(sr[q4][e + 1]));
+          mq[q4] = fmaxf(m, __uint_as_float(sr[q4][31]));
+        }
+        const float m_new = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * c_j;
+        move = m_new > m_ref + kRescaleThreshold;
+        if (move) {
+          corr = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
+          m_ref = m_new;
+          exp_pass(-m_ref);
+        } else if (m_ref == -INFINITY) {
+          exp_pass(0.f);  // no key of the row met yet: every s is -inf and p = 0
         }
       }
-      float sum_lo, sum_hi;
-      f2_split(add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3])), sum_lo, sum_hi);
-      l = l * corr + (sum_lo + sum_hi) / r_j;
+      l = l * corr + sum / r_j;
 
       // P buffer pb was last read by P(j-2) V_{j-2}; o~ is rescaled in place (when this
       // warp's rows moved their reference) only once P(j-1) V_{j-1} has completed
