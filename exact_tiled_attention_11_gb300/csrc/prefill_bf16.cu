@@ -13,14 +13,14 @@
 //     S_c(j) = Q_c K_j^T -> softmax_c(j) -> P_c(j) -> O_c += P_c(j) V_j
 // over Nq query rows and Nk keys; with causal masking query row i attends
 // keys j <= i + (Nk - Nq), i.e. the mask is aligned to the last key (for
-// self-attention, Nq = Nk, this is j <= i).
-// and, because P lives in shared memory rather than over S, S_c(j+1) can be
-// computed as soon as softmax has loaded S_c(j) into registers: the tensor
-// core works on the next score tile (and on the other chain) while the
-// exponentials of this one are evaluated (the FlashAttention-3 overlap, here
-// with tcgen05, tensor memory and TMA).
+// self-attention, Nq = Nk, this is j <= i).  Because P lives in shared
+// memory rather than over S, S_c(j+1) can be computed as soon as softmax has
+// loaded S_c(j) into registers: the tensor core works on the next score tile
+// (and on the other chain) while the exponentials of this one are evaluated
+// (the FlashAttention-3 overlap, here with tcgen05, tensor memory and TMA).
 //   warp 0      TMA: Q_A, Q_B once, then K_j into a 2-stage ring
-//   warp 2      TMA: V_j into a single stage (it is needed only after softmax)
+//   warp 2      TMA: V_j into a single stage (it is needed only after softmax;
+//               V_{j+1} is prefetched into L2 meanwhile)
 //   warp 1      allocates tensor memory and issues every MMA from an elected
 //               lane of the converged warp, polling both chains and issuing
 //               whichever next MMA is ready:
@@ -37,6 +37,9 @@
 //               <= 256), and at the end write O = o~ / l and the LSE.
 // Tensor memory, 512 columns: S_A [0,128), S_B [128,256), O_A [256,256+d),
 // O_B [384,384+d).  Query-tile pairs are ordered heaviest causal pair first.
+// One kernel instance per sequence layout: dense [B, heads, N, d] blocks,
+// ragged token-major tensors with indptr offsets, or ragged queries against
+// a paged K/V cache (each 128-key tile gathered as eight 16-token pages).
 #include <algorithm>
 
 #include "common.cuh"
@@ -339,7 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         load_kv_tile(smem_u32(sm.v), &tm_v, vbar, j, keep, pages);
         ++issued;
         // V has one stage, so each tile's copy waits for the previous tile's P V:
-        // start bringing the next tile into L2 now (dense and ragged layouts)
+        // start bringing the next tile into L2 now (dense and ragged layouts; for
+        // the paged layout the extra page-id loads and per-page prefetches cost more
+        // than they save)
         if (!kPagedK && j + 1 < n_kv) {
 #pragma unroll
           for (int x = 0; x < D / 64; ++x) {
