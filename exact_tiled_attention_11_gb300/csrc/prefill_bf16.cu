@@ -21,12 +21,15 @@
 //   warp 0      TMA: Q_A, Q_B once, then K_j into a 2-stage ring
 //   warp 2      TMA: V_j into a single stage (it is needed only after softmax;
 //               V_{j+1} is prefetched into L2 meanwhile)
-//   warp 1      allocates tensor memory and issues every MMA from an elected
-//               lane of the converged warp, polling both chains and issuing
-//               whichever next MMA is ready:
+//   warps 1, 3  one MMA warp per chain (warp 1 also allocates tensor memory):
+//               an elected lane of the converged warp issues its chain's MMAs
+//               in the order S_c(0), S_c(1), P_c(0) V_0, S_c(2), P_c(1) V_1, ...
 //                 S_c = Q_c K_j^T  (SS; Q, K K-major in SMEM; D in TMEM)
 //                 O_c += P_c V_j   (SS; P K-major, V MN-major in SMEM; D in TMEM)
-//               completion tracked by tcgen05.commit on mbarriers.
+//               after bounded blocking waits on mbarriers; completion is tracked
+//               by tcgen05.commit.  Issuing a group of MMAs blocks while the
+//               tensor pipe holds earlier groups, so a separate issuer per
+//               chain keeps one chain's issue from holding up the other's.
 //   warps 4-7   softmax warpgroup of tile A, warps 8-11 of tile B; one thread
 //               per query row (= TMEM lane): load S, release it, mask, row
 //               max, p = 2^(s' - m), row sum, write P = bf16(p) (round to
@@ -65,10 +68,10 @@ struct PrefillSmem {
   alignas(1024) uint8_t v[kTileBytes];
   alignas(1024) uint8_t p[2][BM * BN * 2];  // P_A, P_B: 128 rows x 128 keys bf16, two 64-key swizzled boxes
   uint64_t q_full;
-  uint64_t k_full[kKStages], k_empty[kKStages];
-  uint64_t v_full, v_empty;
+  uint64_t k_full[kKStages], k_empty[2][kKStages];  // empty: per chain, committed by its MMA warp
+  uint64_t v_full, v_empty[2];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
-  uint64_t mma_done;
+  uint64_t mma_done[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -101,19 +104,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
-}
-
-// Non-blocking test of an mbarrier phase.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
 }
 
 // One lane of a converged warp (the MMA instructions are issued by it while
@@ -229,17 +219,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm.q_full), 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(smem_u32(&sm.k_full[s]), 1);
-      mbar_init(smem_u32(&sm.k_empty[s]), 1);
+      mbar_init(smem_u32(&sm.k_empty[0][s]), 1);
+      mbar_init(smem_u32(&sm.k_empty[1][s]), 1);
     }
     mbar_init(smem_u32(&sm.v_full), 1);
-    mbar_init(smem_u32(&sm.v_empty), 1);
+    mbar_init(smem_u32(&sm.v_empty[0]), 1);
+    mbar_init(smem_u32(&sm.v_empty[1]), 1);
     for (int c = 0; c < 2; ++c) {
       mbar_init(smem_u32(&sm.s_full[c]), 1);
       mbar_init(smem_u32(&sm.s_free[c]), 128);
       mbar_init(smem_u32(&sm.p_full[c]), 128);
       mbar_init(smem_u32(&sm.pv_done[c]), 1);
     }
-    mbar_init(smem_u32(&sm.mma_done), 1);
+    mbar_init(smem_u32(&sm.mma_done[0]), 1);
+    mbar_init(smem_u32(&sm.mma_done[1]), 1);
     sm.abort = 0;
     fence_barrier_init();
   }
@@ -253,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
 
   // Register split: the CTA is launched with 384 threads x 168 registers =
-  // 64,512.  Warpgroup 0 (TMA warps, MMA warp, one idle warp) gives up to
+  // 64,512.  Warpgroup 0 (two TMA warps, two MMA warps) gives up to
   // 56 per thread and the two softmax warpgroups take 224:
   // 128 x 56 + 256 x 224 = 64,512, exactly the launch's allocation.
   if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
@@ -311,7 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int ks = j % kKStages;
-        if (j >= kKStages && !mbar_wait(smem_u32(&sm.k_empty[ks]), ((j / kKStages) - 1) & 1, &sm.abort)) break;
+        // the stage's previous tile must have been read by each chain that used it
+        bool free_ok = true;
+        for (int c = 0; c < 2 && free_ok; ++c)
+          if (j >= kKStages && j - kKStages < n_tiles[c])
+            free_ok = mbar_wait(smem_u32(&sm.k_empty[c][ks]), ((j / kKStages) - 1) & 1, &sm.abort);
+        if (!free_ok) break;
         int pages[8];
         tile_pages(j, pages);
         const uint32_t kbar = smem_u32(&sm.k_full[ks]);
@@ -336,7 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n_kv; ++j) {
         int pages[8];
         tile_pages(j, pages);  // before the wait: the ids do not depend on the stage
-        if (j >= 1 && !mbar_wait(smem_u32(&sm.v_empty), (j - 1) & 1, &sm.abort)) break;
+        bool free_ok = true;
+        for (int c = 0; c < 2 && free_ok; ++c)
+          if (j >= 1 && j - 1 < n_tiles[c]) free_ok = mbar_wait(smem_u32(&sm.v_empty[c]), (j - 1) & 1, &sm.abort);
+        if (!free_ok) break;
         const uint32_t vbar = smem_u32(&sm.v_full);
         mbar_arrive_expect_tx(vbar, Smem::kTileBytes);
         load_kv_tile(smem_u32(sm.v), &tm_v, vbar, j, keep, pages);
@@ -358,99 +359,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (issued > 0) mbar_wait(smem_u32(&sm.v_full), (issued - 1) & 1, nullptr);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ================================================================ MMA warp (polls both chains)
+  } else if (warp == 1 || warp == 3) {
+    // ================================================================ MMA warps, one per chain
+    // Warp 1 issues chain A's MMAs and warp 3 chain B's, each in the order
+    //   S_c(0), S_c(1), P_c(0) V_0, S_c(2), P_c(1) V_1, ...
+    // with blocking (bounded) waits: S_c(j) once softmax has taken S_c(j-1) out of
+    // tensor memory and K_j has landed, P_c(j-1) V_{j-1} once P_c(j-1) is written and
+    // V_{j-1} has landed.  A warp blocked in one chain's MMA issue does not hold up
+    // the other chain.
+    const int c = warp == 1 ? 0 : 1;
+    const int n_c = n_tiles[c];
     constexpr uint32_t idesc_qk = tc05::idesc_bf16_f32(BM, BN, false);
     constexpr uint32_t idesc_pv = tc05::idesc_bf16_f32(BM, D, true);
-    int qk_next[2] = {0, 0};    // next S_c(j) to issue
-    int pv_next[2] = {0, 0};    // next O_c += P_c(j) V_j to issue
-    int k_rel = 0, v_rel = 0;   // next K stage / V tile to hand back to the producers
     bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.q_full), 0, &sm.abort));
     tc05::fence_after_sync();
-    unsigned long long t_idle = 0;
-    uint32_t spins = 0;
-    // lane 0's view of a barrier phase, shared so that the warp stays converged
-    auto ready = [&](uint64_t *bar, uint32_t parity) -> bool {
-      return __shfl_sync(0xffffffffu, mbar_test(smem_u32(bar), parity) ? 1 : 0, 0) != 0;
-    };
-    while (ok && (pv_next[0] < n_tiles[0] || pv_next[1] < n_tiles[1])) {
-      bool progressed = false;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        // S_c(j) = Q_c K_j^T, once softmax has taken S_c(j-1) out of tensor memory
-        const int jq = qk_next[c];
-        if (jq < n_tiles[c] && (jq == 0 || ready(&sm.s_free[c], (jq - 1) & 1)) &&
-            ready(&sm.k_full[jq % kKStages], (jq / kKStages) & 1)) {
-          tc05::fence_after_sync();
-          const uint32_t q_addr = smem_u32(sm.q[c]);
-          const uint32_t k_addr = smem_u32(sm.k[jq % kKStages]);
+    const uint32_t q_addr = smem_u32(sm.q[c]);
+    const uint32_t p_addr = smem_u32(sm.p[c]);
+    const uint32_t v_addr = smem_u32(sm.v);
+    for (int j = 0; ok && j <= n_c; ++j) {
+      if (j < n_c) {
+        const int ks = j % kKStages;
+        ok = __all_sync(0xffffffffu, (j == 0 || mbar_wait(smem_u32(&sm.s_free[c]), (j - 1) & 1, &sm.abort)) &&
+                                         mbar_wait(smem_u32(&sm.k_full[ks]), (j / kKStages) & 1, &sm.abort));
+        if (!ok) break;
+        tc05::fence_after_sync();
+        const uint32_t k_addr = smem_u32(sm.k[ks]);
+        if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            const uint64_t da = tc05::sdesc_sw128(q_addr + off, 16, 1024);
-            const uint64_t db = tc05::sdesc_sw128(k_addr + off, 16, 1024);
-            if (elect_one()) tc05::mma_ss(tmem + c * BN, da, db, idesc_qk, kk > 0);
-            __syncwarp();
+            tc05::mma_ss(tmem + c * BN, tc05::sdesc_sw128(q_addr + off, 16, 1024),
+                         tc05::sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0);
           }
-          if (elect_one()) tc05::commit(smem_u32(&sm.s_full[c]));
-          __syncwarp();
-          qk_next[c] = jq + 1;
-          progressed = true;
-          // hand back K stages whose every reader has been issued
-          while (k_rel < n_kv && (qk_next[0] > k_rel || k_rel >= n_tiles[0]) &&
-                 (qk_next[1] > k_rel || k_rel >= n_tiles[1])) {
-            if (elect_one()) tc05::commit(smem_u32(&sm.k_empty[k_rel % kKStages]));
-            __syncwarp();
-            ++k_rel;
-          }
+          tc05::commit(smem_u32(&sm.s_full[c]));
+          tc05::commit(smem_u32(&sm.k_empty[c][ks]));
         }
-        // O_c += P_c(j) V_j, once softmax has written P_c(j) and V_j has landed
-        const int jp = pv_next[c];
-        if (jp < qk_next[c] && ready(&sm.p_full[c], jp & 1) && ready(&sm.v_full, jp & 1)) {
-          tc05::fence_after_sync();
-          const uint32_t p_addr = smem_u32(sm.p[c]);
-          const uint32_t v_addr = smem_u32(sm.v);
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t da = tc05::sdesc_sw128(p_addr + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
-            const uint64_t db = tc05::sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024);
-            if (elect_one()) tc05::mma_ss(tmem + 2 * BN + c * BN, da, db, idesc_pv, (jp > 0) || (kk > 0));
-            __syncwarp();
-          }
-          if (elect_one()) tc05::commit(smem_u32(&sm.pv_done[c]));
-          __syncwarp();
-          pv_next[c] = jp + 1;
-          progressed = true;
-          while (v_rel < n_kv && (pv_next[0] > v_rel || v_rel >= n_tiles[0]) &&
-                 (pv_next[1] > v_rel || v_rel >= n_tiles[1])) {
-            if (elect_one()) tc05::commit(smem_u32(&sm.v_empty));
-            __syncwarp();
-            ++v_rel;
-          }
-        }
+        __syncwarp();
       }
-      if (progressed) {
-        spins = 0;
-        t_idle = 0;
-      } else if ((++spins & 255u) == 0u) {
-        // nothing ready for a while: give up after the wait limit, or if another warp did
-        const unsigned long long now = global_timer_ns();
-        if (t_idle == 0) t_idle = now;
-        const bool aborted = *reinterpret_cast<volatile int *>(&sm.abort) != 0;
-        const bool expired = now - t_idle > kWaitLimitNs;
-        if (__shfl_sync(0xffffffffu, (aborted || expired) ? 1 : 0, 0)) {
-          if (lane == 0 && expired && !aborted) {
-            record_device_error(ATTN_DEVERR_WAIT_TIMEOUT);
-            sm.abort = 1;
-          }
-          ok = false;
+      if (j > 0) {
+        const int jp = j - 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_full[c]), jp & 1, &sm.abort) &&
+                                         mbar_wait(smem_u32(&sm.v_full), jp & 1, &sm.abort));
+        if (!ok) break;
+        tc05::fence_after_sync();
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            tc05::mma_ss(tmem + 2 * BN + c * BN,
+                         tc05::sdesc_sw128(p_addr + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+                         tc05::sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_pv, (jp > 0) || (kk > 0));
+          tc05::commit(smem_u32(&sm.pv_done[c]));
+          tc05::commit(smem_u32(&sm.v_empty[c]));
         }
+        __syncwarp();
       }
     }
     // every MMA this warp issued must complete before tensor memory is released
-    if (elect_one()) tc05::commit(smem_u32(&sm.mma_done));
+    if (elect_one()) tc05::commit(smem_u32(&sm.mma_done[c]));
     __syncwarp();
-    mbar_wait(smem_u32(&sm.mma_done), 0, nullptr);
+    mbar_wait(smem_u32(&sm.mma_done[c]), 0, nullptr);
   } else if (warp >= 4) {
     // ================================================================ softmax warpgroups
     asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
@@ -480,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q4 = 0; q4 < 4; ++q4) tc05::tmem_ld_x32(s_addr + q4 * 32, sr[q4]);
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) tc05::tmem_ld_wait(sr[q4]);
-      // S_c is in registers: the MMA warp may compute S_c(j+1) into it now
+      // S_c is in registers: its MMA warp may compute S_c(j+1) into it now
       tc05::fence_before_sync();
       mbar_arrive(smem_u32(&sm.s_free[c]));
 

@@ -11,12 +11,11 @@
 // with the same block-wise online softmax, causal tile skipping, warp roles
 // and tensor-memory plan as the bf16 kernel (prefill_bf16.cu): one CTA per
 // pair of 128-row query tiles, a TMA warp for Q and K (3-stage ring), a TMA
-// warp for V (2-stage ring), an MMA warp polling both chains, and two softmax
+// warp for V (2-stage ring), one MMA warp per chain, and two softmax
 // warpgroups.  The e4m3 tiles are half the bf16 size, which leaves room for two
 // P buffers per chain: softmax writes P(j) while P(j-1) V is still running and
 // waits for that product only when it must rescale o~ (the lazy rescale makes
-// that rare).  The MMA warp tests all of its pending conditions in one round
-// trip (one mbarrier test per lane, one ballot).
+// that rare).
 //
 // V's per-block scale sv_j enters through P: softmax writes
 // p'_j = p * r_j with r_j = sv_j / max_i sv_i <= 1 (a shift of the exponent,
@@ -51,11 +50,11 @@ struct Fp8Smem {
   alignas(1024) uint8_t v[kVStages][kTileBytes];    // V^T tiles: 128 rows (d) x 128 keys
   alignas(1024) uint8_t p[2][kPBufs][kTileBytes];   // P of chains A and B: 128 rows x 128 keys
   uint64_t q_full;
-  uint64_t k_full[kKStages], k_empty[kKStages];
-  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t k_full[kKStages], k_empty[2][kKStages];  // empty: per chain, committed by its MMA warp
+  uint64_t v_full[kVStages], v_empty[2][kVStages];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2][kPBufs], pv_done[2][kPBufs];   // per P buffer, so phases never alias
-  uint64_t mma_done;
+  uint64_t mma_done[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -117,18 +116,6 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
       : "=r"(r)
       : "f"(a), "f"(b), "f"(c), "f"(d));
   return r;
-}
-
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
 }
 
 __device__ __forceinline__ bool elect_one() {
@@ -203,11 +190,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm.q_full), 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(smem_u32(&sm.k_full[s]), 1);
-      mbar_init(smem_u32(&sm.k_empty[s]), 1);
+      mbar_init(smem_u32(&sm.k_empty[0][s]), 1);
+      mbar_init(smem_u32(&sm.k_empty[1][s]), 1);
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(smem_u32(&sm.v_full[s]), 1);
-      mbar_init(smem_u32(&sm.v_empty[s]), 1);
+      mbar_init(smem_u32(&sm.v_empty[0][s]), 1);
+      mbar_init(smem_u32(&sm.v_empty[1][s]), 1);
     }
     for (int c = 0; c < 2; ++c) {
       mbar_init(smem_u32(&sm.s_full[c]), 1);
@@ -217,7 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&sm.pv_done[c][pb]), 1);
       }
     }
-    mbar_init(smem_u32(&sm.mma_done), 1);
+    mbar_init(smem_u32(&sm.mma_done[0]), 1);
+    mbar_init(smem_u32(&sm.mma_done[1]), 1);
     sm.abort = 0;
     fence_barrier_init();
   }
@@ -246,7 +236,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int ks = j % kKStages;
-        if (j >= kKStages && !mbar_wait(smem_u32(&sm.k_empty[ks]), ((j / kKStages) - 1) & 1, &sm.abort)) break;
+        // the stage's previous tile must have been read by each chain that used it
+        bool free_ok = true;
+        for (int c = 0; c < 2 && free_ok; ++c)
+          if (j >= kKStages && j - kKStages < n_tiles[c])
+            free_ok = mbar_wait(smem_u32(&sm.k_empty[c][ks]), ((j / kKStages) - 1) & 1, &sm.abort);
+        if (!free_ok) break;
         const uint32_t kbar = smem_u32(&sm.k_full[ks]);
         mbar_arrive_expect_tx(kbar, kTileBytes);
         tma_load_3d_hint(smem_u32(sm.k[ks]), &tm_k, kbar, 0, j * BN, kv_plane, keep);
@@ -267,7 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int vs = j % kVStages;
-        if (j >= kVStages && !mbar_wait(smem_u32(&sm.v_empty[vs]), ((j / kVStages) - 1) & 1, &sm.abort)) break;
+        bool free_ok = true;
+        for (int c = 0; c < 2 && free_ok; ++c)
+          if (j >= kVStages && j - kVStages < n_tiles[c])
+            free_ok = mbar_wait(smem_u32(&sm.v_empty[c][vs]), ((j / kVStages) - 1) & 1, &sm.abort);
+        if (!free_ok) break;
         const uint32_t vbar = smem_u32(&sm.v_full[vs]);
         mbar_arrive_expect_tx(vbar, kTileBytes);
         tma_load_3d_hint(smem_u32(sm.v[vs]), &tm_vt, vbar, j * BN, 0, kv_plane, keep);
@@ -279,111 +278,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ================================================================ MMA warp (polls both chains)
+  } else if (warp == 1 || warp == 3) {
+    // ================================================================ MMA warps, one per chain
+    // Warp 1 issues chain A's MMAs and warp 3 chain B's, each in the order
+    //   S_c(0), S_c(1), P_c(0) V_0, S_c(2), P_c(1) V_1, ...
+    // after bounded blocking waits: S_c(j) once softmax has taken S_c(j-1) out of
+    // tensor memory and K_j has landed, P_c(j-1) V_{j-1} once P_c(j-1) is written
+    // and V_{j-1} has landed.
+    const int c = warp == 1 ? 0 : 1;
+    const int n_c = n_tiles[c];
     constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);  // N = BN = D = 128 for both products
-    int qk_next[2] = {0, 0};
-    int pv_next[2] = {0, 0};
-    int k_rel = 0, v_rel = 0;
     bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.q_full), 0, &sm.abort));
     tc05::fence_after_sync();
-    unsigned long long t_idle = 0;
-    uint32_t spins = 0;
-    while (ok && (pv_next[0] < n_tiles[0] || pv_next[1] < n_tiles[1])) {
-      // Every condition of this pass in one round trip: lane 4c + 0 tests "S_c free",
-      // 4c + 1 "K ready for S_c", 4c + 2 "P_c written", 4c + 3 "V ready for P_c V".
-      const int cl = (lane >> 2) & 1;
-      const int jq_l = cl ? qk_next[1] : qk_next[0];
-      const int jp_l = cl ? pv_next[1] : pv_next[0];
-      bool r = true;
-      if (lane < 8) {
-        const int kind = lane & 3;
-        uint32_t bar, par;
-        if (kind == 0) {
-          bar = smem_u32(&sm.s_free[cl]);
-          par = (jq_l - 1) & 1;
-        } else if (kind == 1) {
-          bar = smem_u32(&sm.k_full[jq_l % kKStages]);
-          par = (jq_l / kKStages) & 1;
-        } else if (kind == 2) {
-          bar = smem_u32(&sm.p_full[cl][jp_l % kPBufs]);
-          par = (jp_l / kPBufs) & 1;
-        } else {
-          bar = smem_u32(&sm.v_full[jp_l % kVStages]);
-          par = (jp_l / kVStages) & 1;
+    const uint64_t dq = tc05::sdesc_sw128(smem_u32(sm.q[c]), 16, 1024);
+    for (int j = 0; ok && j <= n_c; ++j) {
+      if (j < n_c) {
+        // S_c(j) = Q_c K_j^T
+        const int ks = j % kKStages;
+        ok = __all_sync(0xffffffffu, (j == 0 || mbar_wait(smem_u32(&sm.s_free[c]), (j - 1) & 1, &sm.abort)) &&
+                                         mbar_wait(smem_u32(&sm.k_full[ks]), (j / kKStages) & 1, &sm.abort));
+        if (!ok) break;
+        tc05::fence_after_sync();
+        const uint64_t db = tc05::sdesc_sw128(smem_u32(sm.k[ks]), 16, 1024);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 32; ++kk)  // K = 32 e4m3 elements (32 bytes, descriptor +2) per MMA
+            mma_f8(tmem + c * BN, dq + 2 * kk, db + 2 * kk, idesc, kk > 0);
+          tc05::commit(smem_u32(&sm.s_full[c]));
+          tc05::commit(smem_u32(&sm.k_empty[c][ks]));
         }
-        r = (kind == 0 && jq_l == 0) || mbar_test(bar, par);
+        __syncwarp();
       }
-      const uint32_t rdy = __ballot_sync(0xffffffffu, r);
-      bool progressed = false;
+      if (j > 0) {
+        // O_c += P_c(j-1) V_{j-1}
+        const int jp = j - 1;
+        const int pb = jp % kPBufs, vs = jp % kVStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_full[c][pb]), (jp / kPBufs) & 1, &sm.abort) &&
+                                         mbar_wait(smem_u32(&sm.v_full[vs]), (jp / kVStages) & 1, &sm.abort));
+        if (!ok) break;
+        tc05::fence_after_sync();
+        const uint64_t da = tc05::sdesc_sw128(smem_u32(sm.p[c][pb]), 16, 1024);
+        const uint64_t db = tc05::sdesc_sw128(smem_u32(sm.v[vs]), 16, 1024);
+        if (elect_one()) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        // S_c(j) = Q_c K_j^T, once softmax has taken S_c(j-1) out of tensor memory
-        const int jq = qk_next[c];
-        if (jq < n_tiles[c] && ((rdy >> (4 * c)) & 3u) == 3u) {
-          tc05::fence_after_sync();
-          const uint64_t da = tc05::sdesc_sw128(smem_u32(sm.q[c]), 16, 1024);
-          const uint64_t db = tc05::sdesc_sw128(smem_u32(sm.k[jq % kKStages]), 16, 1024);
-          if (elect_one()) {
-#pragma unroll
-            for (int kk = 0; kk < D / 32; ++kk)  // K = 32 e4m3 elements (32 bytes, descriptor +2) per MMA
-              mma_f8(tmem + c * BN, da + 2 * kk, db + 2 * kk, idesc, kk > 0);
-            tc05::commit(smem_u32(&sm.s_full[c]));
-          }
-          __syncwarp();
-          qk_next[c] = jq + 1;
-          progressed = true;
-          // hand back K stages whose every reader has been issued
-          while (k_rel < n_kv && (qk_next[0] > k_rel || k_rel >= n_tiles[0]) &&
-                 (qk_next[1] > k_rel || k_rel >= n_tiles[1])) {
-            if (elect_one()) tc05::commit(smem_u32(&sm.k_empty[k_rel % kKStages]));
-            __syncwarp();
-            ++k_rel;
-          }
+          for (int kk = 0; kk < BN / 32; ++kk)
+            mma_f8(tmem + 2 * BN + c * BN, da + 2 * kk, db + 2 * kk, idesc, (jp > 0) || (kk > 0));
+          tc05::commit(smem_u32(&sm.pv_done[c][pb]));
+          tc05::commit(smem_u32(&sm.v_empty[c][vs]));
         }
-        // O_c += P_c(j) V_j, once softmax has written P_c(j) (so S_c(j) was issued) and V_j has landed
-        const int jp = pv_next[c];
-        if (jp < n_tiles[c] && ((rdy >> (4 * c + 2)) & 3u) == 3u) {
-          tc05::fence_after_sync();
-          const uint64_t da = tc05::sdesc_sw128(smem_u32(sm.p[c][jp % kPBufs]), 16, 1024);
-          const uint64_t db = tc05::sdesc_sw128(smem_u32(sm.v[jp % kVStages]), 16, 1024);
-          if (elect_one()) {
-#pragma unroll
-            for (int kk = 0; kk < BN / 32; ++kk)
-              mma_f8(tmem + 2 * BN + c * BN, da + 2 * kk, db + 2 * kk, idesc, (jp > 0) || (kk > 0));
-            tc05::commit(smem_u32(&sm.pv_done[c][jp % kPBufs]));
-          }
-          __syncwarp();
-          pv_next[c] = jp + 1;
-          progressed = true;
-          while (v_rel < n_kv && (pv_next[0] > v_rel || v_rel >= n_tiles[0]) &&
-                 (pv_next[1] > v_rel || v_rel >= n_tiles[1])) {
-            if (elect_one()) tc05::commit(smem_u32(&sm.v_empty[v_rel % kVStages]));
-            __syncwarp();
-            ++v_rel;
-          }
-        }
-      }
-      if (progressed) {
-        spins = 0;
-        t_idle = 0;
-      } else if ((++spins & 255u) == 0u) {
-        const unsigned long long now = global_timer_ns();
-        if (t_idle == 0) t_idle = now;
-        const bool aborted = *reinterpret_cast<volatile int *>(&sm.abort) != 0;
-        const bool expired = now - t_idle > kWaitLimitNs;
-        if (__shfl_sync(0xffffffffu, (aborted || expired) ? 1 : 0, 0)) {
-          if (lane == 0 && expired && !aborted) {
-            record_device_error(ATTN_DEVERR_WAIT_TIMEOUT);
-            sm.abort = 1;
-          }
-          ok = false;
-        }
+        __syncwarp();
       }
     }
-    if (elect_one()) tc05::commit(smem_u32(&sm.mma_done));
+    // every MMA this warp issued must complete before tensor memory is released
+    if (elect_one()) tc05::commit(smem_u32(&sm.mma_done[c]));
     __syncwarp();
-    mbar_wait(smem_u32(&sm.mma_done), 0, nullptr);
+    mbar_wait(smem_u32(&sm.mma_done[c]), 0, nullptr);
   } else if (warp >= 4) {
     // ================================================================ softmax warpgroups
     asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
