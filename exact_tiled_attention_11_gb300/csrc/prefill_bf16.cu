@@ -38,6 +38,11 @@
 //               maximum moves only when the row max outgrows it by more than
 //               2^8; the result does not depend on the reference, and p stays
 //               <= 256), and at the end write O = o~ / l and the LSE.
+//               The two warpgroups take turns for the exponentials (an mbarrier
+//               token: A's of tile j after B's of tile j-1, B's of tile j after
+//               A's of tile j), so that one chain's exponentials run while the
+//               other stores P and loads its next S, instead of both competing
+//               for the same sub-partitions' MUFU and issue slots at once.
 // Tensor memory, 512 columns: S_A [0,128), S_B [128,256), O_A [256,256+d),
 // O_B [384,384+d).  Query-tile pairs are ordered heaviest causal pair first.
 // One kernel instance per sequence layout: dense [B, heads, N, d] blocks,
@@ -71,6 +76,7 @@ struct PrefillSmem {
   uint64_t k_full[kKStages], k_empty[2][kKStages];  // empty: per chain, committed by its MMA warp
   uint64_t v_full, v_empty[2];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+  uint64_t turn[2];  // turn[c]: the other chain's softmax has finished its exponentials
   uint64_t mma_done[2];
   uint32_t tmem_base;
   int abort;
@@ -230,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.s_free[c]), 128);
       mbar_init(smem_u32(&sm.p_full[c]), 128);
       mbar_init(smem_u32(&sm.pv_done[c]), 1);
+      mbar_init(smem_u32(&sm.turn[c]), 128);
     }
     mbar_init(smem_u32(&sm.mma_done[0]), 1);
     mbar_init(smem_u32(&sm.mma_done[1]), 1);
@@ -475,6 +482,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 1 when kept (also while the row has met no key at all); 0 on the row's first key
       const float corr = (m_next == m_ref) ? 1.f : ex2_approx(m_ref - m_next);
       m_ref = m_next;
+      // ping-pong: chain A's exponentials of tile j follow chain B's of tile j-1, and
+      // chain B's of tile j follow chain A's of tile j
+      {
+        const int need = c == 0 ? j - 1 : j;  // the other chain's step to wait for
+        if (need >= 0 && need < n_tiles[1 - c] &&
+            !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.turn[c]), need & 1, &sm.abort))) {
+          ok = false;
+          break;
+        }
+      }
 
       // p = 2^(s * scale * log2(e) - m_ref), summed in eight partial sums, packed to bf16
       // (a row that has met no key yet has every s = -inf and takes reference 0: p = 0)
@@ -497,6 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sum_lo, sum_hi;
       f2_split(add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3])), sum_lo, sum_hi);
       l = l * corr + (sum_lo + sum_hi);
+      mbar_arrive(smem_u32(&sm.turn[1 - c]));
 
       // P_c(j-1) V_{j-1} must have completed: it reads the P buffer written below
       // and o~ is rescaled in place
