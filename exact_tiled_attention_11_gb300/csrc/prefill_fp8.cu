@@ -15,7 +15,8 @@
 // warpgroups.  The e4m3 tiles are half the bf16 size, which leaves room for two
 // P buffers per chain: softmax writes P(j) while P(j-1) V is still running and
 // waits for that product only when it must rescale o~ (the lazy rescale makes
-// that rare).
+// that rare).  As in the bf16 kernel, the two softmax warpgroups take turns for
+// their exponentials (an mbarrier token passed after each tile's exponentials).
 //
 // V's per-block scale sv_j enters through P: softmax writes
 // p'_j = p * r_j with r_j = sv_j / max_i sv_i <= 1 (a shift of the exponent,
@@ -54,6 +55,7 @@ struct Fp8Smem {
   uint64_t v_full[kVStages], v_empty[2][kVStages];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2][kPBufs], pv_done[2][kPBufs];   // per P buffer, so phases never alias
+  uint64_t turn[2];  // turn[c]: the other chain's softmax has finished its exponentials
   uint64_t mma_done[2];
   uint32_t tmem_base;
   int abort;
@@ -201,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < 2; ++c) {
       mbar_init(smem_u32(&sm.s_full[c]), 1);
       mbar_init(smem_u32(&sm.s_free[c]), 128);
+      mbar_init(smem_u32(&sm.turn[c]), 128);
       for (int pb = 0; pb < kPBufs; ++pb) {
         mbar_init(smem_u32(&sm.p_full[c][pb]), 128);
         mbar_init(smem_u32(&sm.pv_done[c][pb]), 1);
@@ -424,6 +427,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         f2_split(add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3])), lo, hi);
         sum = lo + hi;
       };
+      // ping-pong: chain A's exponentials of tile j follow chain B's of tile j-1, and
+      // chain B's of tile j follow chain A's of tile j
+      {
+        const int need = c == 0 ? j - 1 : j;  // the other chain's step to wait for
+        if (need >= 0 && need < n_tiles[1 - c] &&
+            !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.turn[c]), need & 1, &sm.abort))) {
+          ok = false;
+          break;
+        }
+      }
       bool need_max = m_ref == -INFINITY;
       if (!need_max) {
         exp_pass(-m_ref);
@@ -451,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       l = l * corr + sum / r_j;
+      mbar_arrive(smem_u32(&sm.turn[1 - c]));
 
       // P buffer pb was last read by P(j-2) V_{j-2}; o~ is rescaled in place (when this
       // warp's rows moved their reference) only once P(j-1) V_{j-1} has completed
