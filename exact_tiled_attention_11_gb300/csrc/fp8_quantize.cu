@@ -10,9 +10,9 @@
 // head with one fp32 scale = amax / 448, and each value is stored as the e4m3
 // code of x / scale (round to nearest even, saturating).
 //
-// One CTA per (tensor, head plane, 128-row block), 256 threads: warp w holds
-// rows 16w .. 16w + 15 of the block, lane l holds columns 4l .. 4l + 3 of each
-// row (d = 128).  The Hadamard transform is the fast Walsh-Hadamard butterfly
+// One CTA per (tensor, head plane, 128-row block), 512 threads (64 registers
+// each, so two CTAs per SM): warp w holds rows 8w .. 8w + 7 of the block, lane l
+// holds columns 4l .. 4l + 3 of each row (d = 128).  The Hadamard transform is the fast Walsh-Hadamard butterfly
 // over the 7 bits of the column index: bits 0-1 inside a lane, bits 2-6 across
 // lanes with shuffles.  The 1/sqrt(d) normalisation does not change the codes
 // (the block's scale absorbs it), so it is only folded into the stored scale.
@@ -26,7 +26,7 @@ namespace {
 
 constexpr int kRows = 128;
 constexpr int kD = 128;
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kRowsPerWarp = kRows / (kThreads / 32);
 constexpr float kE4m3Max = 448.f;
 
@@ -97,12 +97,10 @@ __global__ void __launch_bounds__(kThreads) fp8_quantize_kernel(Fp8QuantJob jq, 
       x[r][1] = a1 + a3, x[r][3] = a1 - a3;
 #pragma unroll
       for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = (lane & m) != 0;
+        // lower lane: x + other, upper lane: other - x; fma with +-1 rounds exactly as the add
+        const float sgn = (lane & m) ? -1.f : 1.f;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float other = __shfl_xor_sync(0xffffffffu, x[r][t], m);
-          x[r][t] = upper ? other - x[r][t] : x[r][t] + other;
-        }
+        for (int t = 0; t < 4; ++t) x[r][t] = fmaf(sgn, x[r][t], __shfl_xor_sync(0xffffffffu, x[r][t], m));
       }
     }
   }
