@@ -16,6 +16,7 @@ from ._lib import (  # noqa: F401
     attn_decode_paged_noalloc,
     attn_decode_workspace_size,
     attn_device_error,
+    attn_selftest_wait_timeout,
     attn_fp8_padded_keys,
     attn_fp8_quantize,
     attn_fwd,

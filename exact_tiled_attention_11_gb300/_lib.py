@@ -87,6 +87,8 @@ def load_library() -> ctypes.CDLL:
         lib.attn_status_string.argtypes = [i32]
         lib.attn_device_error.restype = i32
         lib.attn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+        lib.attn_selftest_wait_timeout.restype = i32
+        lib.attn_selftest_wait_timeout.argtypes = [vp, vp]
         _handle = lib
         return lib
 
@@ -470,3 +472,14 @@ def attn_device_error(clear: bool = False) -> int:
     code = ctypes.c_uint32(0)
     _check("attn_device_error", load_library().attn_device_error(ctypes.byref(code), 1 if clear else 0))
     return int(code.value)
+
+
+def attn_selftest_wait_timeout(device=None, stream=None) -> list:
+    """Run the bounded-wait self-test kernel (about one wait limit of GPU time) and
+    return [gave_up_warp0, gave_up_warp1]; afterwards attn_device_error() carries
+    ATTN_DEVERR_WAIT_TIMEOUT."""
+    device = torch.device("cuda") if device is None else torch.device(device)
+    gave_up = torch.full((2,), -1, dtype=torch.int32, device=device)
+    _check("attn_selftest_wait_timeout",
+           load_library().attn_selftest_wait_timeout(_ptr(gave_up), _stream(stream, gave_up.device)))
+    return [int(x) for x in gave_up.cpu()]

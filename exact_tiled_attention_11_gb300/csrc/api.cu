@@ -564,14 +564,22 @@ attn_status_t merge_partials(const float *m, const float *l, const float *o_tild
 attn_status_t attn_device_error(uint32_t *code, int clear) {
   if (code == nullptr) return ATTN_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
-  unsigned int a = 0, b = 0, c = 0, f = 0;
+  unsigned int a = 0, b = 0, c = 0, f = 0, t = 0;
   if (attn::device_error_decode(&a, clear != 0) != cudaSuccess ||
       attn::device_error_prefill_f32(&b, clear != 0) != cudaSuccess ||
       attn::device_error_prefill_bf16(&c, clear != 0) != cudaSuccess ||
-      attn::device_error_prefill_fp8(&f, clear != 0) != cudaSuccess)
+      attn::device_error_prefill_fp8(&f, clear != 0) != cudaSuccess ||
+      attn::device_error_selftest(&t, clear != 0) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  *code = a | b | c | f;
+  *code = a | b | c | f | t;
   return ATTN_OK;
+}
+
+attn_status_t attn_selftest_wait_timeout(int32_t *gave_up, attn_stream_t stream) {
+  if (gave_up == nullptr) return ATTN_ERR_INVALID_ARG;
+  return attn::launch_wait_timeout_selftest(gave_up, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -98,5 +98,9 @@ cudaError_t device_error_decode(unsigned int *value, bool clear);
 cudaError_t device_error_prefill_f32(unsigned int *value, bool clear);
 cudaError_t device_error_prefill_bf16(unsigned int *value, bool clear);
 cudaError_t device_error_prefill_fp8(unsigned int *value, bool clear);
+cudaError_t device_error_selftest(unsigned int *value, bool clear);
+// one CTA whose two warps wait on mbarriers that nothing arrives on (selftest.cu);
+// gave_up[w] = 1 once warp w's bounded wait has given up
+cudaError_t launch_wait_timeout_selftest(int *gave_up, cudaStream_t stream);
 
 }  // namespace attn

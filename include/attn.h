@@ -374,6 +374,21 @@ const char *attn_status_string(attn_status_t status);
  */
 attn_status_t attn_device_error(uint32_t *code, int clear);
 
+/*
+ * attn_selftest_wait_timeout -- exercise the bounded pipeline waits.  Launches
+ * one CTA on `stream` whose two warps wait on mbarriers that nothing ever
+ * arrives on, through the same bounded wait the attention kernels use.  The
+ * first wait to run out (after about 2 s) records ATTN_DEVERR_WAIT_TIMEOUT and
+ * raises the CTA's abort flag; the other warp then gives up through that flag.
+ * The kernel returns without trapping, so the context stays usable.
+ *   gave_up  [2] int32, device, written with 1 for each warp whose wait gave up
+ *            (0 would mean a barrier completed, which nothing here allows)
+ * Returns ATTN_ERR_INVALID_ARG for a null pointer and ATTN_ERR_CUDA if the
+ * launch failed.  Like every entry point it does not synchronise; read the
+ * error word with attn_device_error afterwards.
+ */
+attn_status_t attn_selftest_wait_timeout(int32_t *gave_up, attn_stream_t stream);
+
 #define ATTN_DEVERR_WAIT_TIMEOUT 0x1u   /* a pipeline wait gave up after its iteration limit */
 #define ATTN_DEVERR_BAD_PAGE     0x2u   /* a page id outside [0, num_pages) was skipped */
 #define ATTN_DEVERR_TMEM_ALLOC   0x4u   /* tensor memory allocation returned an unusable address */
