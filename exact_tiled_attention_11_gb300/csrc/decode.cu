@@ -32,12 +32,22 @@ constexpr int kHalfBytes = kPage * 64 * 2;        // one 64-column block of a K 
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
 // Sizes for head dimension D (64 or 128): a stage holds one page of K and one of V;
-// the ring keeps 64 KiB in flight per CTA whatever D is.
+// the ring keeps 32 KiB in flight per CTA whatever D is (64 KiB measured 7 % slower on
+// the 64-sequence workload: three CTAs per SM either way, set by the registers, but
+// the smaller ring leaves more of each SM's unified L1 / shared storage to the cache).
 template <int D>
 struct DecodeGeom {
   static constexpr int kPageBytes = (D / 64) * kHalfBytes;  // 4 KiB at d = 128
   static constexpr int kStageBytes = 2 * kPageBytes;        // K page + V page
-  static constexpr int kStages = (64 * 1024) / kStageBytes;  // 8 at d = 128, 16 at d = 64
+  static constexpr int kStages = (32 * 1024) / kStageBytes;  // 4 at d = 128, 8 at d = 64
+  // Consumer warp w takes pages w, w + 4, ... and page i uses stage i mod kStages, so
+  // with kStages a multiple of the consumer count every use of a stage falls to the same
+  // warp, which then waits on that stage's barrier phases strictly in order.  Otherwise a
+  // warp could wait on a phase two ahead of the barrier, which a parity wait reports as
+  // already complete.
+  static_assert(kStages % kConsumerWarps == 0, "each ring stage must belong to one consumer warp");
+  // the per-warp output fragments are merged through the (then idle) ring at the end
+  static_assert(kConsumerWarps * 16 * D * 4 <= kStages * kStageBytes, "merge scratch must fit in the ring");
 };
 
 template <int D>
@@ -51,8 +61,8 @@ struct DecodeSmem {
   int abort;
 };
 // The per-warp output fragments are merged through the (then idle) stage
-// buffers: 4 warps x 16 rows x d fp32 (32 KiB at d = 128) <= the ring's 64 KiB.
-static_assert(kConsumerWarps * 16 * 128 * 4 <= 64 * 1024, "merge scratch must fit in the ring");
+// buffers: 4 warps x 16 rows x d fp32 (32 KiB at d = 128), the ring's 32 KiB
+// (checked in DecodeGeom).
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -82,8 +92,10 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
 
 // Rows 0..7 of the MMA tile hold query heads 0..7 of the group, rows 8..15
 // heads 8..15; kHiRows says whether any head lands in rows 8..15 (g > 8).
+// Four CTAs per SM (at most 96 registers a thread, a few spilled) measured 2.7 % faster than
+// three; the instance for groups of more than 8 query heads keeps three (it would spill more).
 template <int D, bool kHiRows>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kHiRows ? 3 : 4)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const __nv_bfloat16 *__restrict__ q, const int32_t *__restrict__ page_table,
                         const int32_t *__restrict__ kv_lens, float *__restrict__ ws_m, float *__restrict__ ws_l,
