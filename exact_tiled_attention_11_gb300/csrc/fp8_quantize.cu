@@ -10,11 +10,12 @@
 // head with one fp32 scale = amax / 448, and each value is stored as the e4m3
 // code of x / scale (round to nearest even, saturating).
 //
-// One CTA per (tensor, head plane, 128-row block), 512 threads (64 registers
-// each, so two CTAs per SM): warp w holds rows 8w .. 8w + 7 of the block, lane l
-// holds columns 4l .. 4l + 3 of each row (d = 128).  The Hadamard transform is the fast Walsh-Hadamard butterfly
-// over the 7 bits of the column index: bits 0-1 inside a lane, bits 2-6 across
-// lanes with shuffles.  The 1/sqrt(d) normalisation does not change the codes
+// One CTA per (tensor, head plane, 128-row block), 512 threads: warp w holds
+// rows 8w .. 8w + 7 of the block, two rows per pass, sixteen lanes per row, lane l
+// columns 8 (l mod 16) .. + 7 (d = 128; one 16-byte load per lane and row).  The
+// Hadamard transform is the fast Walsh-Hadamard butterfly over the 7 bits of the
+// column index: bits 0-2 inside the lane (bits 1-2 on packed f32x2 pairs), bits 3-6
+// across the row's sixteen lanes with shuffles.  The 1/sqrt(d) normalisation does not change the codes
 // (the block's scale absorbs it), so it is only folded into the stored scale.
 // V is written transposed, v8t [plane, d, Nk_pad], so that both MMAs of the
 // attention read K-major operands; keys in [Nk, Nk_pad) are zero.
@@ -42,12 +43,34 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return r;
 }
 
+// packed fp32 pairs (Blackwell f32x2 forms)
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t r, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 __global__ void __launch_bounds__(kThreads) fp8_quantize_kernel(Fp8QuantJob jq, Fp8QuantJob jk, Fp8QuantJob jv,
                                                                  const float *signs, float transform_norm) {
   __shared__ float warp_max[kThreads / 32];
-  __shared__ uint8_t tile[kRows][kD + 4];  // V codes, padded rows for the transposed read
+  __shared__ uint8_t tile[kRows][kD + 4];  // V codes; a 132-byte pitch keeps the column reads conflict-free
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int seg = lane & 15;      // this lane's columns: 8 seg .. 8 seg + 7
+  const int half = lane >> 4;     // which of the pass's two rows
 
   // ---- which tensor and block
   long long id = blockIdx.x;
@@ -70,46 +93,60 @@ __global__ void __launch_bounds__(kThreads) fp8_quantize_kernel(Fp8QuantJob jq, 
   const int blk = static_cast<int>(id % nb);
   if (plane >= job.planes) return;
 
-  // ---- load 16 rows x 4 columns per lane (rows past N read as zero)
-  float x[kRowsPerWarp][4];
-  float sg[4] = {1.f, 1.f, 1.f, 1.f};
+  // ---- rows 8 warp + 2 p + half (p = 0..3), 8 columns each, times the signs; rows past N read as zero
+  float sg[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
   if (transform) {
-    const float4 s4 = reinterpret_cast<const float4 *>(signs)[lane];
-    sg[0] = s4.x, sg[1] = s4.y, sg[2] = s4.z, sg[3] = s4.w;
+    const float4 s0 = reinterpret_cast<const float4 *>(signs + seg * 8)[0];
+    const float4 s1 = reinterpret_cast<const float4 *>(signs + seg * 8)[1];
+    sg[0] = s0.x, sg[1] = s0.y, sg[2] = s0.z, sg[3] = s0.w, sg[4] = s1.x, sg[5] = s1.y, sg[6] = s1.z, sg[7] = s1.w;
   }
+  float x[kRowsPerWarp / 2][8];
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int row = blk * kRows + warp * kRowsPerWarp + r;
-    uint2 raw = make_uint2(0u, 0u);
-    if (row < job.N) raw = reinterpret_cast<const uint2 *>(job.x + (plane * job.N + row) * kD)[lane];
-    x[r][0] = __uint_as_float(raw.x << 16) * sg[0];
-    x[r][1] = __uint_as_float(raw.x & 0xFFFF0000u) * sg[1];
-    x[r][2] = __uint_as_float(raw.y << 16) * sg[2];
-    x[r][3] = __uint_as_float(raw.y & 0xFFFF0000u) * sg[3];
+  for (int p = 0; p < kRowsPerWarp / 2; ++p) {
+    const int row = blk * kRows + warp * kRowsPerWarp + 2 * p + half;
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    if (row < job.N) raw = reinterpret_cast<const uint4 *>(job.x + (plane * job.N + row) * kD)[seg];
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      x[p][2 * k] = __uint_as_float(w[k] << 16) * sg[2 * k];
+      x[p][2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u) * sg[2 * k + 1];
+    }
   }
-  // ---- x diag(signs) H_d: butterflies over column bits 0, 1 (in lane) and 2..6 (across lanes)
+  // ---- x diag(signs) H_d: column bits 0..2 in the lane, bits 3..6 across the row's 16 lanes
   if (transform) {
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      float a0 = x[r][0] + x[r][1], a1 = x[r][0] - x[r][1];
-      float a2 = x[r][2] + x[r][3], a3 = x[r][2] - x[r][3];
-      x[r][0] = a0 + a2, x[r][2] = a0 - a2;
-      x[r][1] = a1 + a3, x[r][3] = a1 - a3;
+    for (int p = 0; p < kRowsPerWarp / 2; ++p) {
 #pragma unroll
-      for (int m = 1; m < 32; m <<= 1) {
+      for (int i = 0; i < 8; i += 2) {  // bit 0
+        const float a = x[p][i], c = x[p][i + 1];
+        x[p][i] = a + c, x[p][i + 1] = a - c;
+      }
+#pragma unroll
+      for (int st = 2; st < 8; st <<= 1) {  // bits 1, 2 on packed pairs (i, i + 1)
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          if (i & st) continue;
+          const uint64_t lo = f2(x[p][i], x[p][i + 1]), hi = f2(x[p][i + st], x[p][i + st + 1]);
+          f2_split(add2(lo, hi), x[p][i], x[p][i + 1]);
+          f2_split(sub2(lo, hi), x[p][i + st], x[p][i + st + 1]);
+        }
+      }
+#pragma unroll
+      for (int m = 1; m < 16; m <<= 1) {  // bits 3..6: lanes seg ^ m of the same row
         // lower lane: x + other, upper lane: other - x; fma with +-1 rounds exactly as the add
-        const float sgn = (lane & m) ? -1.f : 1.f;
+        const float sgn = (seg & m) ? -1.f : 1.f;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) x[r][t] = fmaf(sgn, x[r][t], __shfl_xor_sync(0xffffffffu, x[r][t], m));
+        for (int t = 0; t < 8; ++t) x[p][t] = fmaf(sgn, x[p][t], __shfl_xor_sync(0xffffffffu, x[p][t], m));
       }
     }
   }
   // ---- block amax
   float amax = 0.f;
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r)
+  for (int p = 0; p < kRowsPerWarp / 2; ++p)
 #pragma unroll
-    for (int t = 0; t < 4; ++t) amax = fmaxf(amax, fabsf(x[r][t]));
+    for (int t = 0; t < 8; ++t) amax = fmaxf(amax, fabsf(x[p][t]));
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
   if (lane == 0) warp_max[warp] = amax;
@@ -120,16 +157,19 @@ __global__ void __launch_bounds__(kThreads) fp8_quantize_kernel(Fp8QuantJob jq, 
   const float inv = amax > 0.f ? kE4m3Max / amax : 0.f;
   if (threadIdx.x == 0) job.scale[plane * nb + blk] = amax / kE4m3Max * (transform ? transform_norm : 1.f);
 
-  // ---- codes
+  // ---- codes: 8 bytes per lane and row
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int rr = warp * kRowsPerWarp + r;
-    const int row = blk * kRows + rr;
-    const uint32_t c = pack_e4m3x4(x[r][0] * inv, x[r][1] * inv, x[r][2] * inv, x[r][3] * inv);
+  for (int p = 0; p < kRowsPerWarp / 2; ++p) {
+    const int row_in = warp * kRowsPerWarp + 2 * p + half;
+    const int row = blk * kRows + row_in;
+    const uint32_t c0 = pack_e4m3x4(x[p][0] * inv, x[p][1] * inv, x[p][2] * inv, x[p][3] * inv);
+    const uint32_t c1 = pack_e4m3x4(x[p][4] * inv, x[p][5] * inv, x[p][6] * inv, x[p][7] * inv);
     if (!transposed) {
-      if (row < job.N) reinterpret_cast<uint32_t *>(job.out + (plane * job.N + row) * kD)[lane] = c;
+      if (row < job.N) reinterpret_cast<uint2 *>(job.out + (plane * job.N + row) * kD)[seg] = make_uint2(c0, c1);
     } else {
-      *reinterpret_cast<uint32_t *>(&tile[rr][4 * lane]) = c;
+      uint32_t *t = reinterpret_cast<uint32_t *>(&tile[row_in][8 * seg]);
+      t[0] = c0;
+      t[1] = c1;
     }
   }
   if (!transposed) return;
