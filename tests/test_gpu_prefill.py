@@ -40,8 +40,6 @@ def test_c1_fp32_exact(cuda, q_mult):
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 7, 16, 100, 128, 129, 255, 384])
 def test_small_and_ragged(cuda, N, causal, d, dtype):
-    if dtype == "f32" and N in (128, 384):
-        pytest.skip("fp32 path covered at the other sizes")
     B, H, Hkv = 2, 4, 2
     q, k, v = W.prefill_inputs(B, H, Hkv, N, d, dtype, seed=N * 7 + d)
     scale = 1 / math.sqrt(d)
