@@ -25,7 +25,8 @@
 //               an elected lane of the converged warp issues its chain's MMAs
 //               in the order S_c(0), S_c(1), P_c(0) V_0, S_c(2), P_c(1) V_1, ...
 //                 S_c = Q_c K_j^T  (SS; Q, K K-major in SMEM; D in TMEM)
-//                 O_c += P_c V_j   (SS; P K-major, V MN-major in SMEM; D in TMEM)
+//                 O_c += P_c V_j   (SS; P K-major, V MN-major in SMEM; D in TMEM;
+//                                   TS at d = 64: P in TMEM)
 //               after bounded blocking waits on mbarriers; completion is tracked
 //               by tcgen05.commit.  Issuing a group of MMAs blocks while the
 //               tensor pipe holds earlier groups, so a separate issuer per
@@ -34,7 +35,8 @@
 //               per query row (= TMEM lane): load S, release it, mask, row
 //               max, p = 2^(s' - m), row sum, write P = bf16(p) (round to
 //               nearest even) to shared memory in the 128-byte-swizzled
-//               K-major layout, rescale O in TMEM lazily (the reference
+//               K-major layout (to tensor memory at d = 64), rescale O in
+//               TMEM lazily (the reference
 //               maximum moves only when the row max outgrows it by more than
 //               2^8; the result does not depend on the reference, and p stays
 //               <= 256), and at the end write O = o~ / l and the LSE.
@@ -44,7 +46,12 @@
 //               other stores P and loads its next S, instead of both competing
 //               for the same sub-partitions' MUFU and issue slots at once.
 // Tensor memory, 512 columns: S_A [0,128), S_B [128,256), O_A [256,256+d),
-// O_B [384,384+d).  Query-tile pairs are ordered heaviest causal pair first.
+// O_B [384,384+d).  At d = 64 the columns after each O hold that chain's P
+// (128 keys as 64 columns of packed bf16 pairs, written with tcgen05.st), and
+// P V is the TS form (A from tensor memory): no P round trip through shared
+// memory and no async-proxy fence on the softmax's path.  At d = 128 there is
+// no room beside O, and P goes through shared memory.
+// Query-tile pairs are ordered heaviest causal pair first.
 // One kernel instance per sequence layout: dense [B, heads, N, d] blocks,
 // ragged token-major tensors with indptr offsets, or ragged queries against
 // a paged K/V cache (each 128-key tile gathered as eight 16-token pages).
@@ -162,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kRaggedQ = kLay != kDense;  // query offsets from qo_indptr
   constexpr bool kRaggedK = kLay == kRagged;  // key offsets from kv_indptr (rows-outer K/V maps)
   constexpr bool kPagedK = kLay == kPaged;    // keys gathered page by page
+  constexpr bool kPInTmem = D == 64;          // P_c kept in tensor memory for a TS-form P V
   using Smem = PrefillSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -411,10 +419,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc05::fence_after_sync();
         if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            tc05::mma_ss(tmem + 2 * BN + c * BN,
-                         tc05::sdesc_sw128(p_addr + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
-                         tc05::sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_pv, (jp > 0) || (kk > 0));
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            if (kPInTmem)  // P_c in tensor memory beside O_c: 16 keys = 8 columns of packed bf16 pairs
+              tc05::mma_ts(tmem + 2 * BN + c * BN, tmem + 2 * BN + c * BN + D + kk * 8,
+                           tc05::sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_pv, (jp > 0) || (kk > 0));
+            else
+              tc05::mma_ss(tmem + 2 * BN + c * BN,
+                           tc05::sdesc_sw128(p_addr + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+                           tc05::sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_pv, (jp > 0) || (kk > 0));
+          }
           tc05::commit(smem_u32(&sm.pv_done[c]));
           tc05::commit(smem_u32(&sm.v_empty[c]));
         }
@@ -436,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_addr = tmem + lane_addr + c * BN;
     const uint32_t o_addr = tmem + lane_addr + 2 * BN + c * BN;
+    const uint32_t p_tm = o_addr + D;  // P_c in tensor memory (d = 64: the columns after O_c are free)
     const uint32_t p_row = smem_u32(sm.p[c]) + row * 128;  // this row in each 64-key swizzled box
     const int lim = causal ? min(q_row + shift + 1, Nk) : Nk;  // keys [0, lim) are attended by this row
     const uint64_t scale2 = f2(scale_log2, scale_log2);
@@ -529,14 +543,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q4 = 0; q4 < D / 32; ++q4) rescale_o_chunk(o_addr + q4 * 32, corr);
         }
       }
-      // P row -> shared memory: keys 64x + 8ch .. +7 at chunk ch of box x, chunk index XOR (row mod 8)
+      if (kPInTmem) {
+        // P row -> tensor memory beside O_c: column 32x + k holds keys 64x + 2k, 64x + 2k + 1
+        tc05::tmem_st_x32(p_tm, pr[0]);
+        tc05::tmem_st_x32(p_tm + 32, pr[1]);
+      } else {
+        // P row -> shared memory: keys 64x + 8ch .. +7 at chunk ch of box x, chunk index XOR (row mod 8)
 #pragma unroll
-      for (int x = 0; x < 2; ++x)
+        for (int x = 0; x < 2; ++x)
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          st_shared_v4(p_row + x * kBoxBytes + (((ch ^ row) & 7) << 4), pr[x][4 * ch], pr[x][4 * ch + 1],
-                       pr[x][4 * ch + 2], pr[x][4 * ch + 3]);
-      fence_proxy_async_smem();
+          for (int ch = 0; ch < 8; ++ch)
+            st_shared_v4(p_row + x * kBoxBytes + (((ch ^ row) & 7) << 4), pr[x][4 * ch], pr[x][4 * ch + 1],
+                         pr[x][4 * ch + 2], pr[x][4 * ch + 3]);
+        fence_proxy_async_smem();
+      }
       tc05::tmem_wait_st();
       tc05::fence_before_sync();
       mbar_arrive(smem_u32(&sm.p_full[c]));
