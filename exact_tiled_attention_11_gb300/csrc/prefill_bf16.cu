@@ -319,14 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int ks = j % kKStages;
+        int pages[8];
+        tile_pages(j, pages);  // before the wait: the ids do not depend on the stage
         // the stage's previous tile must have been read by each chain that used it
         bool free_ok = true;
         for (int c = 0; c < 2 && free_ok; ++c)
           if (j >= kKStages && j - kKStages < n_tiles[c])
             free_ok = mbar_wait(smem_u32(&sm.k_empty[c][ks]), ((j / kKStages) - 1) & 1, &sm.abort);
         if (!free_ok) break;
-        int pages[8];
-        tile_pages(j, pages);
         const uint32_t kbar = smem_u32(&sm.k_full[ks]);
         mbar_arrive_expect_tx(kbar, Smem::kTileBytes);
         load_kv_tile(smem_u32(sm.k[ks]), &tm_k, kbar, j, keep, pages);
