@@ -124,6 +124,14 @@ class ClockSampler:
                 "samples": len(rows), "reasons": sorted(reasons)}
 
 
+def probe_mhz(p):
+    """Average SM clock between two attn_clock_probe records (None unless both landed on one SM)."""
+    t0, c0, sm0, ok0, t1, c1, sm1, ok1 = p
+    if ok0 != 1 or ok1 != 1 or sm0 != sm1 or t1 <= t0:
+        return None
+    return round(1000.0 * (c1 - c0) / (t1 - t0), 1)
+
+
 def smi_index(local_rank: int) -> str:
     """nvidia-smi's name for this rank's GPU (CUDA_VISIBLE_DEVICES entries are physical ids or UUIDs)."""
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -432,9 +440,11 @@ def run_ours(args, rank, local_rank, world):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
+    probe = torch.zeros(8, dtype=torch.int64, device=dev)  # two clock probes around the timed region
     with ClockSampler(smi_index(local_rank)) as clk:
         start = torch.cuda.Event(enable_timing=True)
         stop = torch.cuda.Event(enable_timing=True)
+        lib.attn_clock_probe(probe[:4], stream=stream)
         start.record(stream)
         for i in range(args.steps):
             ev[i][0].record(stream)
@@ -443,7 +453,9 @@ def run_ours(args, rank, local_rank, world):
             decode()
             ev[i][2].record(stream)
         stop.record(stream)
+        lib.attn_clock_probe(probe[4:], match=probe[:4], stream=stream)
         torch.cuda.synchronize()
+    timed_mhz = probe_mhz(probe.cpu().tolist())
     barrier(world)
     elapsed_ms = start.elapsed_time(stop)
     pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
@@ -527,6 +539,10 @@ def run_ours(args, rank, local_rank, world):
                 "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": dec_bytes}
     dominant = roof_dec if dec_tot > pre_tot else roof_pre
     clocks = clk.summary()
+    if clocks is not None or timed_mhz is not None:
+        clocks = dict(clocks or {})
+        # average SM clock across exactly the timed region, from the device's own counters
+        clocks["sm_mhz_timed_region"] = timed_mhz
 
     line = {
         "metric": METRIC, "value": pre_tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

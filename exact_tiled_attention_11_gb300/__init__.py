@@ -17,6 +17,7 @@ from ._lib import (  # noqa: F401
     attn_decode_workspace_size,
     attn_device_error,
     attn_selftest_wait_timeout,
+    attn_clock_probe,
     attn_fp8_padded_keys,
     attn_fp8_quantize,
     attn_fwd,

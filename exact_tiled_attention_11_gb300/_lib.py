@@ -89,6 +89,8 @@ def load_library() -> ctypes.CDLL:
         lib.attn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         lib.attn_selftest_wait_timeout.restype = i32
         lib.attn_selftest_wait_timeout.argtypes = [vp, vp]
+        lib.attn_clock_probe.restype = i32
+        lib.attn_clock_probe.argtypes = [vp, vp, vp]
         _handle = lib
         return lib
 
@@ -483,3 +485,16 @@ def attn_selftest_wait_timeout(device=None, stream=None) -> list:
     _check("attn_selftest_wait_timeout",
            load_library().attn_selftest_wait_timeout(_ptr(gave_up), _stream(stream, gave_up.device)))
     return [int(x) for x in gave_up.cpu()]
+
+
+def attn_clock_probe(out, match=None, stream=None) -> None:
+    """Queue a clock probe on ``stream``: ``out`` (4 int64 on the device) receives the
+    global timer (ns), one SM's clock64, that SM's id and a claim flag (1 once written).
+    With ``match`` (an earlier probe's ``out``) it records on the same SM.  Two probes
+    around work give its average SM clock: 1000 * d(clock64) / d(timer) MHz."""
+    if not (out.is_cuda and out.dtype == torch.int64 and out.numel() >= 4 and out.is_contiguous()):
+        raise ValueError("attn_clock_probe: out must be a contiguous CUDA int64 tensor of 4 elements")
+    if match is not None and not (match.is_cuda and match.dtype == torch.int64 and match.numel() >= 4):
+        raise ValueError("attn_clock_probe: match must be an earlier probe's output")
+    _check("attn_clock_probe", load_library().attn_clock_probe(_ptr(out), None if match is None else _ptr(match),
+                                                               _stream(stream, out.device)))

@@ -582,4 +582,16 @@ attn_status_t attn_selftest_wait_timeout(int32_t *gave_up, attn_stream_t stream)
              : ATTN_ERR_CUDA;
 }
 
+attn_status_t attn_clock_probe(uint64_t *out, const uint64_t *match, attn_stream_t stream) {
+  if (out == nullptr || (reinterpret_cast<uintptr_t>(out) & 7u) != 0 ||
+      (match != nullptr && (reinterpret_cast<uintptr_t>(match) & 7u) != 0))
+    return ATTN_ERR_INVALID_ARG;
+  const int blocks = 16 * std::max(device_sm_count(), 1);  // every SM gets blocks
+  return attn::launch_clock_probe(reinterpret_cast<unsigned long long *>(out),
+                                  reinterpret_cast<const unsigned long long *>(match), blocks,
+                                  reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_CUDA;
+}
+
 }  // extern "C"

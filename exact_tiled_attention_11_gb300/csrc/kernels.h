@@ -102,5 +102,8 @@ cudaError_t device_error_selftest(unsigned int *value, bool clear);
 // one CTA whose two warps wait on mbarriers that nothing arrives on (selftest.cu);
 // gave_up[w] = 1 once warp w's bounded wait has given up
 cudaError_t launch_wait_timeout_selftest(int *gave_up, cudaStream_t stream);
+// {globaltimer, clock64, smid} of one SM (the SM of `match`'s probe when given); selftest.cu
+cudaError_t launch_clock_probe(unsigned long long *out, const unsigned long long *match, int blocks,
+                               cudaStream_t stream);
 
 }  // namespace attn

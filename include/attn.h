@@ -389,6 +389,21 @@ attn_status_t attn_device_error(uint32_t *code, int clear);
  */
 attn_status_t attn_selftest_wait_timeout(int32_t *gave_up, attn_stream_t stream);
 
+/*
+ * attn_clock_probe -- the SM clock over a stretch of work, measured on the device
+ * (a diagnostic; no counterpart on the pages).  Records, on `stream`, the global
+ * timer (ns) and one SM's cycle counter %clock64:
+ *   out    [4] uint64, device, 8-byte aligned: {global timer ns, clock64, SM id, claim};
+ *          zeroed by the call, then written by the first probe block on the chosen SM
+ *          (claim = 1 once written; 0 means no block ran there)
+ *   match  NULL: any SM; or an earlier probe's `out` (read on the device when this
+ *          probe runs): record on the same SM, since clock64 is a per-SM counter
+ * Two probes around work on one stream give its average SM clock in MHz:
+ * 1000 * (clock64 difference) / (timer difference).  Returns ATTN_ERR_INVALID_ARG
+ * for a null or misaligned pointer, ATTN_ERR_CUDA if the launch failed.
+ */
+attn_status_t attn_clock_probe(uint64_t *out, const uint64_t *match, attn_stream_t stream);
+
 #define ATTN_DEVERR_WAIT_TIMEOUT 0x1u   /* a pipeline wait gave up after its iteration limit */
 #define ATTN_DEVERR_BAD_PAGE     0x2u   /* a page id outside [0, num_pages) was skipped */
 #define ATTN_DEVERR_TMEM_ALLOC   0x4u   /* tensor memory allocation returned an unusable address */

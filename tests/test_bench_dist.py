@@ -63,3 +63,13 @@ def test_smi_index(monkeypatch, vis, rank, want):
     else:
         monkeypatch.setenv("CUDA_VISIBLE_DEVICES", vis)
     assert bench.smi_index(rank) == want
+
+
+def test_probe_mhz_from_two_clock_probes():
+    """The timed region's SM clock from two probe records {timer ns, clock64, SM id, claim}."""
+    import bench
+    # 2.07e9 cycles in 1 s on SM 5
+    assert bench.probe_mhz([1_000_000_000, 10, 5, 1, 2_000_000_000, 10 + 2_070_000_000, 5, 1]) == 2070.0
+    assert bench.probe_mhz([0, 0, 5, 1, 1000, 1500, 6, 1]) is None      # different SMs: counters differ
+    assert bench.probe_mhz([0, 0, 5, 0, 1000, 1500, 5, 1]) is None      # a probe that never ran
+    assert bench.probe_mhz([1000, 0, 5, 1, 1000, 1500, 5, 1]) is None   # no time elapsed
