@@ -78,7 +78,9 @@ struct PrefillSmem {
   alignas(1024) uint8_t q[2][BM * D * 2];
   alignas(1024) uint8_t k[kKStages][kTileBytes];
   alignas(1024) uint8_t v[kTileBytes];
-  alignas(1024) uint8_t p[2][BM * BN * 2];  // P_A, P_B: 128 rows x 128 keys bf16, two 64-key swizzled boxes
+  // P_A, P_B: 128 rows x 128 keys bf16, two 64-key swizzled boxes (at d = 64 P lives in
+  // tensor memory and these are placeholders)
+  alignas(1024) uint8_t p[2][D == 64 ? 1024 : BM * BN * 2];
   uint64_t q_full;
   uint64_t k_full[kKStages], k_empty[2][kKStages];  // empty: per chain, committed by its MMA warp
   uint64_t v_full, v_empty[2];
