@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libattn.so")
 
 SOURCES = ("api.cu", "decode.cu", "prefill_f32.cu", "prefill_bf16.cu", "decode_noalloc.cu", "prefill_fp8.cu",
-           "fp8_quantize.cu", "selftest.cu")
+           "fp8_quantize.cu", "selftest.cu", "cascade.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
                      f"-I{INCLUDE}", f"-I{CSRC}"]

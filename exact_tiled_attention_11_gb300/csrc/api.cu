@@ -73,6 +73,9 @@ int device_sm_count() {
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
+// The shared prefix of a cascade decode runs as at most this many key chunks.
+constexpr int kMaxPrefixChunks = 16;
+
 // Split-KV plan from arguments only (no device-to-host copy): chunks of at
 // most 256 pages (2 MiB of one KV head's K and V at d = 128, long enough to
 // amortise a CTA's set-up), more splits when that gives fewer than ~6 CTAs per
@@ -497,7 +500,9 @@ attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *
 size_t attn_cascade_workspace_size(int B, int H, int d, int max_splits) {
   if (B <= 0 || H <= 0 || d <= 0 || max_splits <= 0) return 0;
   const size_t rows = static_cast<size_t>(B) * H;
-  return decode_ws_bytes(B, H, d, max_splits) + align256(rows * d * 2) + align256(rows * sizeof(float));
+  // the decode partials, the merged prefix partial, and up to kMaxPrefixChunks chunk partials
+  return decode_ws_bytes(B, H, d, max_splits) + (1 + kMaxPrefixChunks) * (align256(rows * d * 2) +
+                                                                          align256(rows * sizeof(float)));
 }
 
 attn_status_t attn_cascade_decode(const void *q, const void *prefix_k, const void *prefix_v, int prefix_len,
@@ -519,27 +524,42 @@ attn_status_t attn_cascade_decode(const void *q, const void *prefix_k, const voi
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
   const size_t rows = static_cast<size_t>(B) * H;
+  const size_t o_bytes = align256(rows * d * 2), l_bytes = align256(rows * sizeof(float));
   char *prefix_area = static_cast<char *>(workspace) + decode_ws_bytes(B, H, d, plan.splits);
-  void *o_prefix = prefix_area;                                                         // [B, H, d] bf16
-  float *lse_prefix = reinterpret_cast<float *>(prefix_area + align256(rows * d * 2));  // [B, H] fp32
+  void *o_prefix = prefix_area;                                         // [B, H, d] bf16
+  float *lse_prefix = reinterpret_cast<float *>(prefix_area + o_bytes);  // [B, H] fp32
+  char *chunk_area = prefix_area + o_bytes + l_bytes;
+  void *o_chunks = chunk_area;                                                                  // [C][B, H, d]
+  float *lse_chunks = reinterpret_cast<float *>(chunk_area + kMaxPrefixChunks * o_bytes);       // [C][B, H]
   if (prefix_len > 0) {
-    // The shared prefix once for every request: one attention whose query rows
-    // are the B requests' tokens (per head), against the prefix keys.
+    // The shared prefix once for every request: attention whose query rows are the B
+    // requests' tokens (per head) against the prefix keys, in C chunks of keys (about
+    // two CTAs per SM in all), each a normalised partial, then merged into one.
+    const int q_tiles = ceil_div(ceil_div(B, 128), 2);  // query-tile pairs per head
+    const int want = ceil_div(2LL * std::max(device_sm_count(), 1), static_cast<long long>(H) * q_tiles);
+    const int key_tiles = ceil_div(prefix_len, 128);
+    const int c_try = std::max(1, std::min({want, key_tiles, kMaxPrefixChunks}));
+    const int chunk = ceil_div(key_tiles, c_try) * 128;
+    const int C = ceil_div(prefix_len, chunk);
     PrefillMaps maps;
     maps.q_rows_outer = true;  // q [B, H, d] seen as (d, H, B): the rows (requests) are the outer dimension
     if (!make_map_3d(&maps.q, q, d, H, B, 1, 128) || !make_map_3d(&maps.k, prefix_k, d, prefix_len, Hkv, 128) ||
         !make_map_3d(&maps.v, prefix_v, d, prefix_len, Hkv, 128))
       return ATTN_ERR_CUDA;
     PrefillOut out;
-    out.o = o_prefix;
-    out.lse = lse_prefix;
-    out.o_b = 0;
+    out.o = o_chunks;
+    out.lse = lse_chunks;
+    out.o_b = static_cast<long long>(o_bytes / 2);  // chunk stride
     out.o_h = d;
     out.o_r = static_cast<long long>(H) * d;
-    out.l_b = 0;
+    out.l_b = static_cast<long long>(l_bytes / sizeof(float));
     out.l_h = 1;
     out.l_r = H;
-    if (attn::launch_prefill_bf16(maps, out, 1, H, Hkv, B, prefix_len, d, false, scale, st) != cudaSuccess)
+    attn::PrefillLayout lay;
+    lay.key_chunk = chunk;
+    if (attn::launch_prefill_bf16(maps, out, C, H, Hkv, B, prefix_len, d, false, scale, st, lay) != cudaSuccess ||
+        attn::launch_merge_chunks(o_chunks, lse_chunks, C, static_cast<int>(rows), out.o_b, out.l_b, d, o_prefix,
+                                  lse_prefix, st) != cudaSuccess)
       return ATTN_ERR_CUDA;
   }
   // each request's own suffix, merged with the prefix result as one more partial

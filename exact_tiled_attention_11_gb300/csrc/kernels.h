@@ -51,7 +51,11 @@ struct PrefillMaps {
 //  * paged (qo_indptr and kv_lens): ragged queries; keys are the kv_lens[b] tokens
 //    gathered through page_table[b, :] from a pool of num_pages pages of 16 tokens,
 //    the K/V maps spanning the pool as (d, 16, num_pages * Hkv).  With max_pages 0 no
-//    page is ever read (page_table may then be null).
+//    page is ever read (page_table may then be null);
+//  * key chunks (key_chunk > 0): one shared set of Nk keys (the dense K/V maps, one plane
+//    per KV head) split into chunks; batch b takes keys [b * key_chunk, (b + 1) *
+//    key_chunk) against the same Nq query rows (rows-outer Q map), and writes its own
+//    normalised O and LSE (a partial for a later merge) at batch stride o_b / l_b.
 struct PrefillLayout {
   const int32_t *qo_indptr = nullptr;
   const int32_t *kv_indptr = nullptr;
@@ -61,7 +65,13 @@ struct PrefillLayout {
   int num_pages = 0;
   int total_q = 0;  // rows of q / o (bounds every indptr range)
   int total_k = 0;  // rows of k / v
+  int key_chunk = 0;  // keys per chunk (key-chunk layout), a multiple of 128
 };
+// cascade.cu: merge C normalised partials (O bf16, partial c at o_parts + c * o_stride
+// elements, rows x d; LSE at lse_parts + c * l_stride) of each row into one (O bf16
+// [rows][d], LSE [rows]); a partial with LSE = -inf weighs nothing
+cudaError_t launch_merge_chunks(const void *o_parts, const float *lse_parts, int C, int rows, long long o_stride,
+                                long long l_stride, int d, void *o, float *lse, cudaStream_t stream);
 cudaError_t launch_prefill_bf16(const PrefillMaps &maps, const PrefillOut &out, int B, int H, int Hkv, int Nq,
                                 int Nk, int d, bool causal, float scale, cudaStream_t stream,
                                 const PrefillLayout &layout = PrefillLayout());

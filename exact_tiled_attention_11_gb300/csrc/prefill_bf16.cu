@@ -160,7 +160,7 @@ __device__ __forceinline__ void rescale_o_chunk(uint32_t taddr, float corr) {
 
 // Where each sequence's rows live: one dense block per (batch, head), ragged
 // (indptr offsets into token-major q/k/v), or ragged queries against a paged cache.
-enum { kDense = 0, kRagged = 1, kPaged = 2 };
+enum { kDense = 0, kRagged = 1, kPaged = 2, kKeyChunks = 3 };
 
 template <int D, int kLay>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -168,7 +168,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tm_v, const PrefillOut out, const PrefillLayout lay,
                         int B, int H, int Hkv, int Nq_max, int Nk_dense, int causal, float scale_log2,
                         int q_rows_outer) {
-  constexpr bool kRaggedQ = kLay != kDense;  // query offsets from qo_indptr
+  constexpr bool kRaggedQ = kLay != kDense;  // query rows are the outer dimension (q_plane = head)
+  constexpr bool kIndptrQ = kLay == kRagged || kLay == kPaged;  // query offsets from qo_indptr
+  constexpr bool kChunkK = kLay == kKeyChunks;  // batch b: keys [b * key_chunk, ...) of one shared set
   constexpr bool kRaggedK = kLay == kRagged;  // key offsets from kv_indptr (rows-outer K/V maps)
   constexpr bool kPagedK = kLay == kPaged;    // keys gathered page by page
   constexpr bool kPInTmem = D == 64;          // P_c kept in tensor memory for a TS-form P V
@@ -194,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // reads the same values, so the whole CTA leaves together.
   int Nq = Nq_max, Nk = Nk_dense, q_base = 0, k_base = 0;
   bool bad = false;
-  if (kRaggedQ) {
+  if (kIndptrQ) {
     q_base = lay.qo_indptr[b];
     Nq = lay.qo_indptr[b + 1] - q_base;
     bad |= q_base < 0 || Nq < 0 || Nq > Nq_max || static_cast<long long>(q_base) + Nq > lay.total_q;
@@ -208,6 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (t == 0 && threadIdx.x == 0) record_device_error(ATTN_DEVERR_BAD_LENGTH);
     return;
   }
+  if (kChunkK) {
+    k_base = b * lay.key_chunk;
+    Nk = max(0, min(lay.key_chunk, Nk_dense - k_base));
+  }
   if (kPagedK) {
     Nk = lay.kv_lens[b];
     if (Nk < 0 || Nk > lay.max_pages * 16) {  // beyond the table: clamped, as in paged decode
@@ -217,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (2 * t * BM >= Nq) return;  // this pair lies past the sequence's queries
   const int q_plane = kRaggedQ ? h : b * H + h;
-  const int kv_plane = kRaggedK ? kvh : b * Hkv + kvh;
+  const int kv_plane = (kRaggedK || kChunkK) ? kvh : b * Hkv + kvh;
   const int row0[2] = {2 * t * BM, (2 * t + 1) * BM};
   const bool has_b = row0[1] < Nq;
   const int n_kt_all = (Nk + BN - 1) / BN;
@@ -278,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kRaggedK)
           tma_load_3d_hint(dst + x * kBoxBytes, map, bar, x * 64, kv_plane, k_base + j * BN, policy);
         else
-          tma_load_3d_hint(dst + x * kBoxBytes, map, bar, x * 64, j * BN, kv_plane, policy);
+          tma_load_3d_hint(dst + x * kBoxBytes, map, bar, x * 64, k_base + j * BN, kv_plane, policy);
       } else {
 #pragma unroll
         for (int pg = 0; pg < 8; ++pg)
@@ -369,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kRaggedK)
               tma_prefetch_l2(&tm_v, x * 64, kv_plane, k_base + (j + 1) * BN);
             else
-              tma_prefetch_l2(&tm_v, x * 64, (j + 1) * BN, kv_plane);
+              tma_prefetch_l2(&tm_v, x * 64, k_base + (j + 1) * BN, kv_plane);
           }
         }
       }
@@ -636,6 +642,7 @@ cudaError_t launch_d(const PrefillMaps &maps, const PrefillOut &out, const Prefi
 template <int D>
 cudaError_t launch_layout(const PrefillMaps &maps, const PrefillOut &out, const PrefillLayout &lay, int B, int H,
                           int Hkv, int Nq, int Nk, bool causal, float scale, cudaStream_t stream) {
+  if (lay.key_chunk > 0) return launch_d<D, kKeyChunks>(maps, out, lay, B, H, Hkv, Nq, Nk, causal, scale, stream);
   if (lay.kv_lens != nullptr) return launch_d<D, kPaged>(maps, out, lay, B, H, Hkv, Nq, Nk, causal, scale, stream);
   if (lay.kv_indptr != nullptr) return launch_d<D, kRagged>(maps, out, lay, B, H, Hkv, Nq, Nk, causal, scale, stream);
   return launch_d<D, kDense>(maps, out, lay, B, H, Hkv, Nq, Nk, causal, scale, stream);
