@@ -53,8 +53,10 @@
 // no room beside O, and P goes through shared memory.
 // Query-tile pairs are ordered heaviest causal pair first.
 // One kernel instance per sequence layout: dense [B, heads, N, d] blocks,
-// ragged token-major tensors with indptr offsets, or ragged queries against
-// a paged K/V cache (each 128-key tile gathered as eight 16-token pages).
+// ragged token-major tensors with indptr offsets, ragged queries against
+// a paged K/V cache (each 128-key tile gathered as eight 16-token pages), or
+// one shared key set split into chunks, each chunk a partial for a later merge
+// (the shared prefix of cascade decode).
 #include <algorithm>
 
 #include "common.cuh"
