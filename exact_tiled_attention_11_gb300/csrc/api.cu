@@ -500,9 +500,10 @@ attn_status_t attn_decode_paged(const void *q, const void *k_pages, const void *
 size_t attn_cascade_workspace_size(int B, int H, int d, int max_splits) {
   if (B <= 0 || H <= 0 || d <= 0 || max_splits <= 0) return 0;
   const size_t rows = static_cast<size_t>(B) * H;
-  // the decode partials, the merged prefix partial, and up to kMaxPrefixChunks chunk partials
-  return decode_ws_bytes(B, H, d, max_splits) + (1 + kMaxPrefixChunks) * (align256(rows * d * 2) +
-                                                                          align256(rows * sizeof(float)));
+  // the decode partials, the merged prefix partial, up to kMaxPrefixChunks chunk partials,
+  // and the queries regrouped by KV head
+  return decode_ws_bytes(B, H, d, max_splits) +
+         (1 + kMaxPrefixChunks) * (align256(rows * d * 2) + align256(rows * sizeof(float))) + align256(rows * d * 2);
 }
 
 attn_status_t attn_cascade_decode(const void *q, const void *prefix_k, const void *prefix_v, int prefix_len,
@@ -530,36 +531,42 @@ attn_status_t attn_cascade_decode(const void *q, const void *prefix_k, const voi
   float *lse_prefix = reinterpret_cast<float *>(prefix_area + o_bytes);  // [B, H] fp32
   char *chunk_area = prefix_area + o_bytes + l_bytes;
   void *o_chunks = chunk_area;                                                                  // [C][B, H, d]
-  float *lse_chunks = reinterpret_cast<float *>(chunk_area + kMaxPrefixChunks * o_bytes);       // [C][B, H]
+  float *lse_chunks = reinterpret_cast<float *>(chunk_area + kMaxPrefixChunks * o_bytes);       // [C][Hkv, B * g]
+  void *q_grouped = chunk_area + kMaxPrefixChunks * (o_bytes + l_bytes);                        // [Hkv][B * g][d]
   if (prefix_len > 0) {
-    // The shared prefix once for every request: attention whose query rows are the B
-    // requests' tokens (per head) against the prefix keys, in C chunks of keys (about
-    // two CTAs per SM in all), each a normalised partial, then merged into one.
-    const int q_tiles = ceil_div(ceil_div(B, 128), 2);  // query-tile pairs per head
-    const int want = ceil_div(2LL * std::max(device_sm_count(), 1), static_cast<long long>(H) * q_tiles);
+    // The shared prefix once for every request: per KV head, one attention whose query
+    // rows are the B requests' g query heads of that group (B * g rows) against the
+    // prefix keys, in C chunks of keys (about two CTAs per SM in all), each a
+    // normalised partial, then merged into one.
+    const int g = H / Hkv;
+    const int q_tiles = ceil_div(ceil_div(static_cast<long long>(B) * g, 128), 2);  // query-tile pairs per KV head
+    const int want = ceil_div(2LL * std::max(device_sm_count(), 1), static_cast<long long>(Hkv) * q_tiles);
     const int key_tiles = ceil_div(prefix_len, 128);
     const int c_try = std::max(1, std::min({want, key_tiles, kMaxPrefixChunks}));
     const int chunk = ceil_div(key_tiles, c_try) * 128;
     const int C = ceil_div(prefix_len, chunk);
-    PrefillMaps maps;
-    maps.q_rows_outer = true;  // q [B, H, d] seen as (d, H, B): the rows (requests) are the outer dimension
-    if (!make_map_3d(&maps.q, q, d, H, B, 1, 128) || !make_map_3d(&maps.k, prefix_k, d, prefix_len, Hkv, 128) ||
+    const int group_rows = B * g;
+    PrefillMaps maps;  // Q planes are the KV heads, each with its B * g query rows
+    if (!make_map_3d(&maps.q, q_grouped, d, group_rows, Hkv, 128) ||
+        !make_map_3d(&maps.k, prefix_k, d, prefix_len, Hkv, 128) ||
         !make_map_3d(&maps.v, prefix_v, d, prefix_len, Hkv, 128))
       return ATTN_ERR_CUDA;
-    PrefillOut out;
+    PrefillOut out;  // chunk partials [C][Hkv][B * g][d] and [C][Hkv][B * g]
     out.o = o_chunks;
     out.lse = lse_chunks;
-    out.o_b = static_cast<long long>(o_bytes / 2);  // chunk stride
-    out.o_h = d;
-    out.o_r = static_cast<long long>(H) * d;
+    out.o_b = static_cast<long long>(o_bytes / 2);
+    out.o_h = static_cast<long long>(group_rows) * d;
+    out.o_r = d;
     out.l_b = static_cast<long long>(l_bytes / sizeof(float));
-    out.l_h = 1;
-    out.l_r = H;
+    out.l_h = group_rows;
+    out.l_r = 1;
     attn::PrefillLayout lay;
     lay.key_chunk = chunk;
-    if (attn::launch_prefill_bf16(maps, out, C, H, Hkv, B, prefix_len, d, false, scale, st, lay) != cudaSuccess ||
-        attn::launch_merge_chunks(o_chunks, lse_chunks, C, static_cast<int>(rows), out.o_b, out.l_b, d, o_prefix,
-                                  lse_prefix, st) != cudaSuccess)
+    if (attn::launch_group_queries(q, q_grouped, B, H, Hkv, d, st) != cudaSuccess ||
+        attn::launch_prefill_bf16(maps, out, C, Hkv, Hkv, group_rows, prefix_len, d, false, scale, st, lay) !=
+            cudaSuccess ||
+        attn::launch_merge_chunks(o_chunks, lse_chunks, C, static_cast<int>(rows), out.o_b, out.l_b, B, g, d,
+                                  o_prefix, lse_prefix, st) != cudaSuccess)
       return ATTN_ERR_CUDA;
   }
   // each request's own suffix, merged with the prefix result as one more partial

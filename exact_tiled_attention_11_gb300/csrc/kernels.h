@@ -67,11 +67,13 @@ struct PrefillLayout {
   int total_k = 0;  // rows of k / v
   int key_chunk = 0;  // keys per chunk (key-chunk layout), a multiple of 128
 };
+// cascade.cu: q [B, H, d] bf16 -> qg [Hkv][B * g][d] (the query rows of each KV head)
+cudaError_t launch_group_queries(const void *q, void *qg, int B, int H, int Hkv, int d, cudaStream_t stream);
 // cascade.cu: merge C normalised partials (O bf16, partial c at o_parts + c * o_stride
-// elements, rows x d; LSE at lse_parts + c * l_stride) of each row into one (O bf16
-// [rows][d], LSE [rows]); a partial with LSE = -inf weighs nothing
+// elements, rows x d in the [Hkv][B * g] row order; LSE at lse_parts + c * l_stride) of
+// each row into one (O bf16 [B, H, d], LSE [B, H]); a partial with LSE = -inf weighs nothing
 cudaError_t launch_merge_chunks(const void *o_parts, const float *lse_parts, int C, int rows, long long o_stride,
-                                long long l_stride, int d, void *o, float *lse, cudaStream_t stream);
+                                long long l_stride, int B, int g, int d, void *o, float *lse, cudaStream_t stream);
 cudaError_t launch_prefill_bf16(const PrefillMaps &maps, const PrefillOut &out, int B, int H, int Hkv, int Nq,
                                 int Nk, int d, bool causal, float scale, cudaStream_t stream,
                                 const PrefillLayout &layout = PrefillLayout());
