@@ -274,8 +274,8 @@ int attn_decode_max_splits(int B, int H, int Hkv, int max_pages_per_seq);
 /*
  * attn_cascade_workspace_size -- bytes of device workspace attn_cascade_decode
  * needs: the decode partials for max_splits chunks, the shared-prefix result
- * (bf16 O [B, H, d] and fp32 LSE [B, H]) and up to 16 key-chunk partials of the
- * same shape, each region 256-byte aligned.
+ * (bf16 O [B, H, d] and fp32 LSE [B, H]), up to 16 key-chunk partials of the
+ * same shape and a copy of q grouped by KV head, each region 256-byte aligned.
  * Returns 0 for invalid arguments.
  */
 size_t attn_cascade_workspace_size(int B, int H, int d, int max_splits);
@@ -288,10 +288,11 @@ size_t attn_cascade_workspace_size(int B, int H, int d, int max_splits);
  * (attention over the shared prefix is computed once for all requests' queries
  * and merged with each request's own-suffix attention by the merge operator)
  * and "Check your understanding" (attention over prefix U suffix is the
- * log-sum-exp merge of the two).  The prefix pass is attention whose query
- * rows are the B requests' tokens (per head) against the prefix keys, on the
- * tensor-core prefill kernel, split into up to 16 chunks of keys (about two
- * CTAs per SM) whose normalised partials are merged into one prefix result;
+ * log-sum-exp merge of the two).  The prefix pass is attention, per KV head,
+ * whose query rows are the B requests' query heads of that head's group,
+ * against the prefix keys, on the tensor-core prefill kernel, split into up to
+ * 16 chunks of keys (about two CTAs per SM) whose normalised partials are
+ * merged into one prefix result;
  * the suffix pass is attn_decode_paged's split kernel; the merge kernel
  * combines the suffix chunks' partials with the prefix result taken as the
  * partial (m, l, o~) = (LSE_prefix, 1, O_prefix).
