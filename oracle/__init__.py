@@ -13,7 +13,10 @@ that it can be checked against the pages by eye:
 
 * ``attention``        -- the plain definition (materialised S, stable softmax,
                           P.V, log-sum-exp), which exact tiled attention reaches
-                          up to rounding order.
+                          up to rounding order; ``attention_weights`` returns
+                          the softmax weights P of selected rows (the error
+                          bound of FP8 attention weighs each key's rounding by
+                          them).
 * ``tiled_attention``  -- the block-wise algorithm itself (online softmax over
                           K/V tiles, causal tile skipping), reporting the block
                           pairs it visited.
@@ -42,6 +45,7 @@ unpinned.
 from .attention import (  # noqa: F401
     attention,
     attention_rows,
+    attention_weights,
     tiled_attention,
     partial_state,
     merge_partials,

@@ -55,28 +55,63 @@ def _causal_keep(rows: np.ndarray, Nk: int, N: int) -> np.ndarray:
     return cols[None, :] <= (rows[:, None] + (Nk - N))
 
 
-def _softmax_rows(S: np.ndarray, Vh: np.ndarray):
-    """Stable softmax of each row of S (entries may be -inf), then P V.
+def _softmax_weights(S: np.ndarray):
+    """Stable softmax of each row of S (entries may be -inf).
 
-    m = rowmax S, P = exp(S - m), l = sum P, O = P V / l, LSE = m + ln l.
-    Rows whose every entry is -inf attend to nothing: O = 0, LSE = -inf.
+    m = rowmax S, E = exp(S - m), l = sum E, P = E / l, LSE = m + ln l.
+    Rows whose every entry is -inf attend to nothing: P = 0, LSE = -inf.
+    Returns (P [rows, Nk], LSE [rows]).
     """
     n_rows = S.shape[0]
-    O = np.zeros((n_rows, Vh.shape[1]))
+    P = np.zeros(S.shape)
     lse = np.full(n_rows, -np.inf)
     if S.shape[1] == 0 or n_rows == 0:
-        return O, lse
+        return P, lse
     m = S.max(axis=1)
     live = np.isfinite(m)
     if not live.any():
-        return O, lse
-    Sl = S[live]
+        return P, lse
     ml = m[live]
-    P = np.exp(Sl - ml[:, None])          # exp(-inf) = 0 for masked keys
-    l = P.sum(axis=1)
-    O[live] = (P @ Vh) / l[:, None]
+    E = np.exp(S[live] - ml[:, None])     # exp(-inf) = 0 for masked keys
+    l = E.sum(axis=1)
+    P[live] = E / l[:, None]
     lse[live] = ml + np.log(l)
-    return O, lse
+    return P, lse
+
+
+def _softmax_rows(S: np.ndarray, Vh: np.ndarray):
+    """The softmax weights of S applied to V: O = P V, LSE as in _softmax_weights.
+
+    Rows that attend to nothing have P = 0, so O = 0 and LSE = -inf.
+    """
+    P, lse = _softmax_weights(S)
+    return P @ Vh, lse
+
+
+def _scores(Q, K, b: int, h: int, rows, *, causal: bool, scale: float):
+    """S = scale * q K^T for query rows ``rows`` of head (b, h) against KV head
+    h // (H / Hkv), keys after the query set to -inf when causal."""
+    H, N = Q.shape[1], Q.shape[2]
+    Hkv, Nk = K.shape[1], K.shape[2]
+    kvh = h // (H // Hkv)
+    rows = np.asarray(rows, dtype=np.int64)
+    q = to_f64(Q[b, h])[rows]
+    Kh = to_f64(K[b, kvh])
+    S = scale * (q @ Kh.T)                 # [rows, Nk], materialised
+    if causal:
+        S = np.where(_causal_keep(rows, Nk, N), S, -np.inf)
+    return S
+
+
+def attention_weights(Q, K, b: int, h: int, rows, *, causal: bool, scale: float):
+    """The softmax weights P = softmax(scale q K^T) of query rows ``rows`` of head (b, h).
+
+    Q: [B, H, N, d], K: [B, Hkv, Nk, d].  Row i of P holds the weight of every
+    key in row i's output, O_i = sum_j P_ij V_j; masked keys have weight 0 and
+    a row with no attended key is all zero.  Returns (P [len(rows), Nk],
+    LSE [len(rows)]) in float64.
+    """
+    return _softmax_weights(_scores(Q, K, b, h, rows, causal=causal, scale=scale))
 
 
 def attention_rows(Q, K, V, b: int, h: int, rows, *, causal: bool, scale: float):
@@ -85,17 +120,9 @@ def attention_rows(Q, K, V, b: int, h: int, rows, *, causal: bool, scale: float)
     Q: [B, H, N, d], K/V: [B, Hkv, Nk, d] (any float dtype; upcast to float64).
     Returns (O [len(rows), d], LSE [len(rows)]) in float64.
     """
-    H, N = Q.shape[1], Q.shape[2]
-    Hkv, Nk = K.shape[1], K.shape[2]
-    kvh = h // (H // Hkv)
-    rows = np.asarray(rows, dtype=np.int64)
-    q = to_f64(Q[b, h])[rows]
-    Kh = to_f64(K[b, kvh])
-    Vh = to_f64(V[b, kvh])
-    S = scale * (q @ Kh.T)                 # [rows, Nk], materialised
-    if causal:
-        S = np.where(_causal_keep(rows, Nk, N), S, -np.inf)
-    return _softmax_rows(S, Vh)
+    H, Hkv = Q.shape[1], K.shape[1]
+    Vh = to_f64(V[b, h // (H // Hkv)])
+    return _softmax_rows(_scores(Q, K, b, h, rows, causal=causal, scale=scale), Vh)
 
 
 def attention(Q, K, V, *, causal: bool, scale: float, row_chunk: int = 2048):

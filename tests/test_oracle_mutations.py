@@ -113,3 +113,56 @@ def test_pins_catch_merge_without_rescale(monkeypatch):
     monkeypatch.setattr(oracle, "merge_partials", bad_merge)
     assert _fails(pins.test_p4_worked_example_block_states)
     assert _fails(pins.test_invariant_b_merge_any_partition_order_association, 7)
+
+
+def _varlen_swapped(orig):
+    def swapped(q, k, v, qo_indptr, kv_indptr, *, causal, scale):
+        return orig(q, k, v, kv_indptr, qo_indptr, causal=causal, scale=scale)
+    return swapped
+
+
+def _varlen_keys_by_query_offsets(q, k, v, qo_indptr, kv_indptr, *, causal, scale):
+    """Slices each sequence's keys with the query offsets (a plausible copy-paste slip)."""
+    return _ORIG_VARLEN(q, k, v, qo_indptr, qo_indptr, causal=causal, scale=scale)
+
+
+_ORIG_VARLEN = ORC.varlen_attention
+
+
+@pytest.mark.parametrize("mutant", ["swapped", "keys_by_query_offsets"])
+def test_unequal_length_pin_catches_indptr_mistakes(monkeypatch, mutant):
+    """Swapped or mis-sliced indptr arrays pass the equal-length pin (both arrays are
+    the same there) and fail the pin with unequal query and key lengths."""
+    fn = _varlen_swapped(_ORIG_VARLEN) if mutant == "swapped" else _varlen_keys_by_query_offsets
+    monkeypatch.setattr(ORC, "varlen_attention", fn)
+    monkeypatch.setattr(oracle, "varlen_attention", fn)
+    assert not _fails(pins.test_varlen_equal_lengths_is_dense_attention)
+    assert _fails(pins.test_varlen_unequal_lengths_brute_force, False) or \
+        _fails(pins.test_varlen_unequal_lengths_brute_force, True)
+
+
+def _weights_unnormalised(S):
+    P, lse = _ORIG_WEIGHTS(S)
+    return P * 1.5, lse
+
+
+def _weights_transposed_mask(S):
+    n, Nk = S.shape
+    if n == Nk:
+        S = np.where(np.isneginf(S), S.T, S)
+    return _ORIG_WEIGHTS(S)
+
+
+def _weights_base2(S):
+    return _ORIG_WEIGHTS(S / np.log(2.0))
+
+
+_ORIG_WEIGHTS = ORC._softmax_weights
+
+
+@pytest.mark.parametrize("fn", [_weights_unnormalised, _weights_transposed_mask, _weights_base2])
+def test_weight_pins_catch_planted_mistake(monkeypatch, fn):
+    monkeypatch.setattr(ORC, "_softmax_weights", fn)
+    caught = _fails(pins.test_attention_weights_brute_force, 6, 6, 2, 1, True) or \
+        _fails(pins.test_attention_weights_closed_form_zero_keys)
+    assert caught, f"no pin caught {fn.__name__}"

@@ -70,6 +70,25 @@ def brute_attention(Q, K, V, causal, scale):
     return O, LSE
 
 
+def brute_weights(q_rows, keys, causal, scale, shift):
+    """Softmax weights of each query row over the keys, by scalar loops.
+
+    q_rows: [n][d] lists, keys: [Nk][d]; row i attends key j when not causal or
+    j <= i + shift.  Returns [n][Nk] lists (all zeros for a row with no key)."""
+    W = []
+    for i, q in enumerate(q_rows):
+        keep = [j for j in range(len(keys)) if (not causal) or j <= i + shift]
+        row = [0.0] * len(keys)
+        if keep:
+            s = {j: scale * sum(a * b for a, b in zip(q, keys[j])) for j in keep}
+            top = max(s.values())
+            z = sum(math.exp(s[j] - top) for j in keep)
+            for j in keep:
+                row[j] = math.exp(s[j] - top) / z
+        W.append(row)
+    return W
+
+
 def _rand(shape, rng):
     return rng.standard_normal(shape)
 
@@ -482,6 +501,75 @@ def test_varlen_equal_lengths_is_dense_attention():
         Ov, Lv = oracle.varlen_attention(q, k, v, indptr, indptr, causal=causal, scale=0.4)
         np.testing.assert_allclose(Ov, O.transpose(0, 2, 1, 3).reshape(B * N, H, d), rtol=0, atol=1e-12)
         np.testing.assert_allclose(Lv, LSE.transpose(0, 2, 1).reshape(B * N, H), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_unequal_lengths_brute_force(causal):
+    """Ragged batch whose query and key lengths differ per sequence (Lq < Lk, Lq > Lk,
+    Lq = 0, Lk = 0, Lq = Lk), each sequence checked against the scalar brute force on
+    its own slices: query rows [qo_indptr[b], qo_indptr[b+1]) against key rows
+    [kv_indptr[b], kv_indptr[b+1]), the causal mask aligned to the sequence's last key.
+    A sequence with queries but no keys has O = 0 and LSE = -inf."""
+    rng = np.random.default_rng(73)
+    H, Hkv, d = 4, 2, 5
+    q_lens = [3, 0, 6, 2, 4, 1]
+    k_lens = [7, 4, 2, 0, 4, 9]
+    qo = np.concatenate([[0], np.cumsum(q_lens)])
+    kvp = np.concatenate([[0], np.cumsum(k_lens)])
+    q = rng.standard_normal((qo[-1], H, d))
+    k = rng.standard_normal((kvp[-1], Hkv, d))
+    v = rng.standard_normal((kvp[-1], Hkv, d))
+    O, LSE = oracle.varlen_attention(q, k, v, qo, kvp, causal=causal, scale=0.45)
+    assert O.shape == (qo[-1], H, d) and LSE.shape == (qo[-1], H)
+    for b in range(len(q_lens)):
+        rows = slice(qo[b], qo[b + 1])
+        if q_lens[b] == 0:
+            continue
+        if k_lens[b] == 0:
+            assert (O[rows] == 0).all() and np.isneginf(LSE[rows]).all()
+            continue
+        Qb = [[q[rows, h].tolist() for h in range(H)]]
+        Kb = [[k[kvp[b]:kvp[b + 1], g].tolist() for g in range(Hkv)]]
+        Vb = [[v[kvp[b]:kvp[b + 1], g].tolist() for g in range(Hkv)]]
+        Ob, Lb = brute_attention(Qb, Kb, Vb, causal, 0.45)
+        np.testing.assert_allclose(O[rows], np.array(Ob[0]).transpose(1, 0, 2), rtol=0, atol=1e-12)
+        Lb = np.array(Lb[0]).T
+        np.testing.assert_array_equal(np.isneginf(LSE[rows]), np.isneginf(Lb))
+        fin = np.isfinite(Lb)
+        np.testing.assert_allclose(LSE[rows][fin], Lb[fin], rtol=0, atol=1e-12)
+    if causal:  # sequence 2 has 6 queries and 2 keys: its first 4 rows attend nothing
+        assert np.isneginf(LSE[qo[2]:qo[2] + 4]).all() and (O[qo[2]:qo[2] + 4] == 0).all()
+        assert np.isfinite(LSE[qo[2] + 4:qo[3]]).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,Nk,H,Hkv", [(1, 1, 1, 1), (6, 6, 2, 1), (4, 9, 4, 2), (9, 4, 2, 2), (17, 17, 1, 1)])
+def test_attention_weights_brute_force(N, Nk, H, Hkv, causal):
+    """oracle.attention_weights against the scalar softmax weights, head by head (GQA,
+    cross shapes with the mask aligned to the last key)."""
+    rng = np.random.default_rng(N * 31 + Nk * 7 + H + causal)
+    d = 6
+    Q = rng.standard_normal((1, H, N, d)) * 2.0
+    K = rng.standard_normal((1, Hkv, Nk, d))
+    rows = np.arange(N)
+    for h in range(H):
+        P, LSE = oracle.attention_weights(Q, K, 0, h, rows, causal=causal, scale=0.6)
+        Wb = np.array(brute_weights(Q[0, h].tolist(), K[0, h // (H // Hkv)].tolist(), causal, 0.6, Nk - N))
+        np.testing.assert_allclose(P, Wb, rtol=0, atol=1e-14)
+        live = Wb.sum(axis=1) > 0
+        np.testing.assert_allclose(P[live].sum(axis=1), 1.0, rtol=0, atol=1e-14)
+        assert np.isneginf(LSE[~live]).all() and np.isfinite(LSE[live]).all()
+
+
+def test_attention_weights_closed_form_zero_keys():
+    """K = 0: causal row i weighs its i + 1 keys equally, non-causal rows weigh all N keys equally."""
+    Q = np.random.default_rng(5).standard_normal((1, 1, 7, 4))
+    K = np.zeros((1, 1, 7, 4))
+    P, _ = oracle.attention_weights(Q, K, 0, 0, np.arange(7), causal=True, scale=1.0)
+    expect = np.tril(np.ones((7, 7))) / np.arange(1, 8)[:, None]
+    np.testing.assert_allclose(P, expect, rtol=0, atol=1e-15)
+    P, _ = oracle.attention_weights(Q, K, 0, 0, np.arange(7), causal=False, scale=1.0)
+    np.testing.assert_allclose(P, np.full((7, 7), 1 / 7), rtol=0, atol=1e-15)
 
 
 def test_paged_prefill_brute_force():
