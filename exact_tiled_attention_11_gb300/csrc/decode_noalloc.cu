@@ -27,7 +27,9 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 // Device address of g_decode_scratch, per device.  In host code the name
 // g_decode_scratch is only a host-side stand-in for the symbol, never a
 // device address; the real address comes from cudaGetSymbolAddress with the
-// device current.
+// device current.  It is looked up once per device and kept, so it is valid
+// only while that device's primary context lives (no cudaDeviceReset between
+// calls).
 constexpr int kMaxDevices = 128;
 std::mutex g_mutex;
 void *g_scratch_addr[kMaxDevices] = {};

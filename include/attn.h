@@ -355,7 +355,10 @@ attn_status_t merge_partials(const float *m, const float *l, const float *o_tild
  *
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress, with the caller's current device); make that
- * first call before any stream capture.  All calls on a device share the one
+ * first call before any stream capture.  The address is kept for the life of
+ * the process: after cudaDeviceReset, or any other end of the device's
+ * primary context, it no longer names the array, so no call may follow such a
+ * reset on that device.  All calls on a device share the one
  * array and it keeps the previous call's contents; nothing in it needs to
  * start at zero, because every partial the merge reads is written earlier in
  * the same call.  Calls that overlap on the GPU (on different streams, or

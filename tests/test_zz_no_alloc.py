@@ -4,15 +4,17 @@ Such callers (a plugin or custom op that another runtime hands only its input an
 output buffers, or a serving loop that must not call cudaMalloc because it can
 synchronise the device) get the same decode with the partials kept in a fixed
 device array of the library.  These checks call the entry point through the C
-ABI and compare it with attn_decode_paged given an ordinary workspace, on two
-calls in a row so that the second call runs on the scratch contents the first
-one left behind.
+ABI and compare it with attn_decode_paged given an ordinary workspace and with
+the float64 oracle, on two calls in a row so that the second call runs on the
+scratch contents the first one left behind.
 """
 import ctypes
 import math
 
 import pytest
 import torch
+
+import oracle
 
 from exact_tiled_attention_11_gb300 import attn_decode_paged, load_library
 from exact_tiled_attention_11_gb300 import workloads as W
@@ -48,6 +50,9 @@ def test_noalloc_matches_workspace_decode_on_two_calls(cuda):
         torch.cuda.synchronize()
         check_o(o.cpu(), o_ref.cpu(), torch.bfloat16, f"noalloc splits={splits}")
         check_lse(lse.cpu(), lse_ref.cpu(), f"noalloc splits={splits}")
+        O, L = oracle.decode_paged(kv.q, kv.k_pages, kv.v_pages, kv.page_table, kv.kv_lens, scale=1.0 / math.sqrt(d))
+        check_o(o.cpu(), O, torch.bfloat16, f"noalloc vs oracle splits={splits}")
+        check_lse(lse.cpu(), L, f"noalloc vs oracle splits={splits}")
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(cuda):
