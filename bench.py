@@ -9,6 +9,11 @@ full-size synthetic workload, with inputs resident in HBM:
            permutation of the pool (split kernel + merge kernel)
 ``value`` is the prefill throughput in TFLOP/s (4 N^2 d B H / 2 for causal),
 the decode throughput is reported in GB/s beside it, each with its roofline.
+``configs`` adds every workload of the suite timed on its own (fp32 N=256 d=64
+with Q x1 and x30; bf16 B=4 H=12 N=2048 d=64 causal and non-causal; bf16
+B=2 H=16 N=16384 d=128 causal with Q x1 and x40; the step's two halves), each
+with its roofline fraction, the SM clock across its launches and the float64
+oracle's host time on a sample of the same inputs.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 With --gpus N > 1 it runs under torch.distributed.run, one independent replica
@@ -303,6 +308,150 @@ def launch_overhead(dev, calls=20, reps=20):
             "eager_us_per_call": eager_us, "graph_us_per_call": graph_us, "calls_per_graph": calls}
 
 
+# ------------------------------------------------------------------ every workload, timed alone
+
+def time_launches(stream, fn, flush, reps, warmup=5):
+    """Event-timed launches of ``fn`` on ``stream``: each between its own pair of CUDA
+    events, an L2-sized write between launches (outside the events).  Returns the
+    sorted per-launch milliseconds."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for e0, e1 in ev:
+        flush.fill_(1)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return sorted(e0.elapsed_time(e1) for e0, e1 in ev)
+
+
+def _timing(ms):
+    return {"ms": statistics.median(ms), "ms_min": ms[0], "ms_max": ms[-1], "n": len(ms)}
+
+
+def oracle_rows_sample(q, k, v, planes, rows, causal, scale):
+    """Time the float64 oracle on sampled query rows of (batch, head) planes; return (flops, seconds)."""
+    import numpy as np
+    import oracle
+    d = q.shape[-1]
+    N, Nk = q.shape[2], k.shape[2]
+    t0 = time.perf_counter()
+    flops = 0.0
+    for b, h in planes:
+        oracle.attention_rows(q, k, v, b, h, rows, causal=causal, scale=scale)
+        keys = np.minimum(rows + 1 + (Nk - N), Nk) if causal else np.full(len(rows), Nk)
+        flops += float(np.sum(4.0 * keys * d))
+    return flops, time.perf_counter() - t0
+
+
+def per_config(dev, stream, t_peak, peak_src, step, baseline, reps=20, with_oracle=True):
+    """Every workload of the benchmark suite on its own: TFLOP/s (4 N^2 d B H, halved
+    for causal) or GB/s, the fraction of the measured roofline, the average SM clock
+    across the timed launches (two on-device clock probes), and the float64 oracle's
+    host time on a bounded sample of the same inputs, extrapolated to the whole
+    workload by its FLOP count.  The long causal prefill (N=8192) and the paged
+    decode come from the benchmark step itself."""
+    import numpy as np
+    import torch
+    import exact_tiled_attention_11_gb300 as lib
+    from exact_tiled_attention_11_gb300 import workloads as W
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    probe = torch.zeros(8, dtype=torch.int64, device=dev)
+    rng = np.random.default_rng(1)
+    out = {}
+
+    def timed(fn):
+        lib.attn_clock_probe(probe[:4], stream=stream)
+        ms = time_launches(stream, fn, flush, reps)
+        lib.attn_clock_probe(probe[4:], match=probe[:4], stream=stream)
+        torch.cuda.synchronize()
+        return ms, probe_mhz(probe.cpu().tolist())
+
+    def oracle_leg(host, cfg, causal, n_planes, n_rows):
+        if not with_oracle:
+            return None
+        planes = [(int(rng.integers(cfg.B)), int(rng.integers(cfg.H))) for _ in range(n_planes)]
+        rows = np.sort(rng.choice(cfg.N, min(n_rows, cfg.N), replace=False))
+        fl, dt = oracle_rows_sample(*host, planes, rows, causal, cfg.scale)
+        rate = fl / dt
+        return {"value": rate / 1e12, "unit": "TFLOP/s", "seconds": dt, "cores": host_cores(), "kind": "oracle",
+                "est_seconds_whole_workload": cfg.flops(causal) / rate,
+                "sample": f"{n_planes} (batch, head) planes x {len(rows)} random query rows ({fl:.3g} FLOP)"}
+
+    # ---- the latency floor: one launch of a kernel that does no work (the clock probe)
+    floor = time_launches(stream, lambda: lib.attn_clock_probe(probe[:4], stream=stream), flush, reps)
+    floor_us = 1e3 * statistics.median(floor)
+
+    # ---- fp32 exact attention, B=1 H=1 N=256 d=64, non-causal, Q x1 and x30
+    for mult in W.C1.q_mults:
+        host = W.prefill_inputs_for(W.C1, q_mult=mult)
+        q, k, v = (t.to(dev) for t in host)
+        o, lse = torch.empty_like(q), torch.empty(1, 1, W.C1.N, dtype=torch.float32, device=dev)
+        ms, mhz = timed(lambda: lib.attn_fwd(q, k, v, o, lse, causal=False, scale=W.C1.scale))
+        t = _timing(ms)
+        tf = W.C1.flops(False) / (t["ms"] * 1e-3) / 1e12
+        out[f"C1 fp32 x{mult:g}"] = {
+            "workload": f"{W.C1.name}, non-causal, Q x{mult:g}", "dtype": "f32", **t, "value": tf,
+            "unit": "TFLOP/s", "bound": "latency", "latency_floor_us": floor_us, "frac": floor_us / (1e3 * t["ms"]),
+            "frac_of": "launch latency floor (event-timed launch of an empty kernel) / this launch",
+            "sm_mhz": mhz, "oracle": oracle_leg(host, W.C1, False, 1, W.C1.N)}
+
+    # ---- bf16 d=64, B=4 H=12 N=2048, causal and non-causal
+    host = W.prefill_inputs_for(W.C2)
+    q, k, v = (t.to(dev) for t in host)
+    o, lse = torch.empty_like(q), torch.empty(W.C2.B, W.C2.H, W.C2.N, dtype=torch.float32, device=dev)
+    for causal in (False, True):
+        ms, mhz = timed(lambda: lib.attn_fwd(q, k, v, o, lse, causal=causal, scale=W.C2.scale))
+        t = _timing(ms)
+        tf = W.C2.flops(causal) / (t["ms"] * 1e-3) / 1e12
+        out[f"C2 bf16 d64 {'causal' if causal else 'non-causal'}"] = {
+            "workload": f"{W.C2.name}, {'causal' if causal else 'non-causal'}", "dtype": "bf16", **t,
+            "value": tf, "unit": "TFLOP/s", "bound": "tensor", "kernel": "prefill_bf16_kernel<64>",
+            "peak": t_peak, "frac": tf / t_peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
+            "sm_mhz": mhz, "oracle": oracle_leg(host, W.C2, causal, 2, 256)}
+    del q, k, v, o, lse
+
+    # ---- the step's own prefill (N=8192 causal GQA) and decode
+    out["C3 bf16 N8192 causal GQA (step)"] = {
+        "workload": W.C3.name, "dtype": "bf16", **_timing(sorted(step["pre_ms"])),
+        "value": step["pre_tflops_median"], "unit": "TFLOP/s", "bound": "tensor",
+        "kernel": "prefill_bf16_kernel<128>", "peak": t_peak, "frac": step["pre_tflops_median"] / t_peak,
+        "sm_mhz": step["mhz"], "note": "inside the benchmark step, after the decode has streamed 4.1 GB",
+        "oracle": baseline.get("prefill") if baseline else None}
+    out["C4 paged decode (step)"] = {
+        "workload": W.C4.name, "dtype": "bf16", **_timing(sorted(step["dec_ms"])),
+        "value": step["dec_gbs_median"], "unit": "GB/s", "bound": "hbm", "peak": step["hbm_peak"],
+        "frac": step["dec_gbs_median"] / step["hbm_peak"], "sm_mhz": step["mhz"],
+        "oracle": baseline.get("decode") if baseline else None}
+
+    # ---- bf16 d=128, B=2 H=16 N=16384 causal, Q x1 and x40
+    kv_dev = None
+    for mult in W.C5.q_mults:
+        host = W.prefill_inputs_for(W.C5, q_mult=mult)
+        q = host[0].to(dev)
+        if kv_dev is None:
+            kv_dev = (host[1].to(dev), host[2].to(dev))
+        k, v = kv_dev
+        o, lse = torch.empty_like(q), torch.empty(W.C5.B, W.C5.H, W.C5.N, dtype=torch.float32, device=dev)
+        ms, mhz = timed(lambda: lib.attn_fwd(q, k, v, o, lse, causal=True, scale=W.C5.scale))
+        t = _timing(ms)
+        tf = W.C5.flops(True) / (t["ms"] * 1e-3) / 1e12
+        out[f"C5 bf16 N16384 causal x{mult:g}"] = {
+            "workload": f"{W.C5.name}, Q x{mult:g}", "dtype": "bf16", **t, "value": tf, "unit": "TFLOP/s",
+            "bound": "tensor", "kernel": "prefill_bf16_kernel<128>", "peak": t_peak, "frac": tf / t_peak,
+            "peak_source": f"{peak_src} bf16_tflops (burst)", "sm_mhz": mhz,
+            "oracle": oracle_leg(host, W.C5, True, 1, 128)}
+        del q, o, lse
+    if lib.attn_device_error() != 0:
+        raise SystemExit("a kernel recorded a device error in the per-workload measurements")
+    return {"timing": (f"each launch between its own CUDA events on the launching stream, {reps} launches after "
+                       f"5 warm-up, median reported; a 256 MiB write between launches (L2 flush)"),
+            "runs": out}
+
+
 # ------------------------------------------------------------------ CPU oracle legs
 
 def oracle_prefill_sample(q, k, v, heads, rows, scale):
@@ -346,12 +495,18 @@ def cpu_baseline(host, kv):
     rows = np.sort(rng.choice(W.C3.N, PREFILL_SAMPLE["rows"], replace=False))
     fl, dt = oracle_prefill_sample(host["q"], host["k"], host["v"], PREFILL_SAMPLE["heads"], rows, W.C3.scale)
     nb, ddt = oracle_decode_sample(kv, DECODE_SAMPLE_SEQS, W.C4.scale)
+    pre_sample = (f"{len(PREFILL_SAMPLE['heads'])} heads x {len(rows)} random query rows of the N=8192 causal "
+                  f"workload ({fl:.3g} algorithmic FLOP)")
+    dec_sample = f"{len(DECODE_SAMPLE_SEQS)} of 64 sequences ({nb / 1e9:.3f} GB of K/V)"
     return {
         "value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
-        "sample": (f"float64 NumPy oracle, prefill: {len(PREFILL_SAMPLE['heads'])} heads x {len(rows)} random query "
-                   f"rows of the N=8192 causal workload ({fl:.3g} algorithmic FLOP in {dt:.2f} s); decode: "
-                   f"{len(DECODE_SAMPLE_SEQS)} of 64 sequences ({nb / 1e9:.3f} GB of K/V in {ddt:.2f} s)"),
-        "decode": {"value": nb / ddt / 1e9, "unit": "GB/s"},
+        "sample": (f"float64 NumPy oracle, prefill: {pre_sample} in {dt:.2f} s; decode: {dec_sample} in "
+                   f"{ddt:.2f} s"),
+        "prefill": {"value": fl / dt / 1e12, "unit": "TFLOP/s", "seconds": dt, "cores": host_cores(),
+                    "kind": "oracle", "est_seconds_whole_workload": W.C3.flops(True) / (fl / dt),
+                    "sample": pre_sample},
+        "decode": {"value": nb / ddt / 1e9, "unit": "GB/s", "seconds": ddt, "cores": host_cores(), "kind": "oracle",
+                   "est_seconds_whole_workload": kv.kv_bytes() / (nb / ddt), "sample": dec_sample},
     }
 
 
@@ -563,8 +718,14 @@ def run_ours(args, rank, local_rank, world):
     }
     line["launch_overhead"] = launch_overhead(dev)
     line["fp8"] = fp8_variant(dev, d, t_peak, hbm_peak)
-    if world == 1 and not args.no_cpu_baseline:
+    with_oracle = world == 1 and not args.no_cpu_baseline
+    if with_oracle:
         line["cpu_baseline"] = cpu_baseline(host, kv)
+    step = {"pre_ms": pre_ms, "dec_ms": dec_ms, "mhz": timed_mhz, "hbm_peak": hbm_peak,
+            "pre_tflops_median": pre_flops / (statistics.median(pre_ms) * 1e-3) / 1e12,
+            "dec_gbs_median": dec_bytes / (statistics.median(dec_ms) * 1e-3) / 1e9}
+    line["configs"] = per_config(dev, stream, t_peak, peak_src, step, line.get("cpu_baseline"),
+                                 with_oracle=with_oracle)
     print(json.dumps(line), flush=True)
     return 0
 
@@ -572,7 +733,8 @@ def run_ours(args, rank, local_rank, world):
 def run_profile_case(args):
     """One kernel family alone, for ncu: W warm-up launches then one more launch.
 
-    prefill: the long causal workload (B=1, H=32, Hkv=8, N=8192, d=128).
+    prefill: a prefill workload (--workload C3: B=1, H=32, Hkv=8, N=8192, d=128
+             causal; C2: B=4, H=12, N=2048, d=64; C5: B=2, H=16, N=16384, d=128).
     fp8:     the same inputs through attn_fp8_quantize + attn_fwd_fp8.
     decode:  the paged decode workload restricted to its first --decode-batch
              sequences (same length distribution and page placement recipe).
@@ -583,9 +745,12 @@ def run_profile_case(args):
     dev = torch.device("cuda", 0)
     lib.load_library()
     if args.profile == "prefill":
-        q, k, v = (t.to(dev) for t in W.prefill_inputs_for(W.C3))
+        cfg = {"C2": W.C2, "C3": W.C3, "C5": W.C5}[args.workload]
+        causal = True if args.causal is None else bool(args.causal)
+        q, k, v = (t.to(dev) for t in W.prefill_inputs_for(cfg, q_mult=args.q_mult))
         for _ in range(args.warmup + 1):
-            lib.attn_fwd(q, k, v, causal=True, scale=W.C3.scale)
+            lib.attn_fwd(q, k, v, causal=causal, scale=cfg.scale)
+        print(f"prefill case: {cfg.name}, causal={causal}, Q x{args.q_mult:g}, {cfg.flops(causal):.4g} FLOP per call")
     elif args.profile == "fp8":
         q, k, v = (t.to(dev) for t in W.prefill_inputs_for(W.C3))
         signs = W.fp8_signs(128).to(dev)
@@ -613,6 +778,10 @@ def main(argv=None):
     ap.add_argument("--profile", choices=["prefill", "decode", "fp8"], default=None,
                     help="run one kernel family alone (for ncu) instead of the benchmark")
     ap.add_argument("--decode-batch", type=int, default=16)
+    ap.add_argument("--workload", choices=["C2", "C3", "C5"], default="C3",
+                    help="--profile prefill: C2 (B4 H12 N2048 d64), C3 (B1 H32/8 N8192 d128), C5 (B2 H16 N16384 d128)")
+    ap.add_argument("--causal", type=int, choices=[0, 1], default=None, help="--profile prefill: causal (default 1)")
+    ap.add_argument("--q-mult", type=float, default=1.0, help="--profile prefill: Q multiplier (30 or 40 stress)")
     args = ap.parse_args(argv)
     if args.profile:
         return run_profile_case(args)
