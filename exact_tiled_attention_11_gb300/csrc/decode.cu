@@ -310,6 +310,24 @@ __global__ void __launch_bounds__(kThreads, kHiRows ? 3 : 4)
       pa[2] = pack_bf16x2(p[1][0], p[1][1]);
       pa[3] = pack_bf16x2(p[1][2], p[1][3]);
 
+      // ---- slots of the sequence's last page past its length may hold anything (stale
+      //      tokens, or non-finite values in a pool that was never written): their weights
+      //      are exact zeros, but 0 x NaN is NaN in the MMA, so their V rows are zeroed first
+      //      (whole 128-byte rows of each 64-column half; the swizzle only permutes chunks
+      //      within a row).  The proxy fence orders these writes before the TMA that later
+      //      refills the stage.
+      const int valid = L - tok0;
+      if (valid < kPage) {
+        const int n16 = (kPage - valid) * 8;  // 16-byte chunks per half
+        for (int idx = lane; idx < n16 * (D / 64); idx += 32) {
+          const int half = idx / n16, rem = idx % n16;
+          *reinterpret_cast<uint4 *>(&sm.stage[s][kPageBytes + half * kHalfBytes + (valid + rem / 8) * 128 +
+                                                  (rem % 8) * 16]) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+      }
+
       // ---- O += P V over the 16 n tiles of the head dimension
 #pragma unroll
       for (int dt = 0; dt < D / 8; dt += 2) {

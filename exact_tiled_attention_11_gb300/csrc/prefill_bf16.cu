@@ -86,6 +86,7 @@ struct PrefillSmem {
   uint64_t q_full;
   uint64_t k_full[kKStages], k_empty[2][kKStages];  // empty: per chain, committed by its MMA warp
   uint64_t v_full, v_empty[2];
+  uint64_t v_tail;   // paged layout: the last V tile with its tail slots zeroed
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
   uint64_t turn[2];  // turn[c]: the other chain's softmax has finished its exponentials
   uint64_t mma_done[2];
@@ -238,6 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   const int n_tiles[2] = {tiles_of(row0[0]), has_b ? tiles_of(row0[1]) : 0};
   const int n_kv = max(n_tiles[0], n_tiles[1]);
+  // paged layout: keys [Nk, Nk rounded up to a page) of the last tile are the unused slots of the
+  // sequence's last page, which may hold anything; their V rows are zeroed before P V reads them
+  // (their weights are exact zeros, but 0 x NaN is NaN in the MMA).  Later pages of the tile read
+  // as zeros already (page id -1 lies outside the pool).
+  const bool v_tail_fix = kPagedK && (Nk % 16) != 0 && n_kv > 0 && (n_kv - 1) * BN < Nk;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm.q_full), 1);
@@ -247,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.k_empty[1][s]), 1);
     }
     mbar_init(smem_u32(&sm.v_full), 1);
+    mbar_init(smem_u32(&sm.v_tail), 1);
     mbar_init(smem_u32(&sm.v_empty[0]), 1);
     mbar_init(smem_u32(&sm.v_empty[1]), 1);
     for (int c = 0; c < 2; ++c) {
@@ -367,6 +374,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(vbar, Smem::kTileBytes);
         load_kv_tile(smem_u32(sm.v), &tm_v, vbar, j, keep, pages);
         ++issued;
+        if (v_tail_fix && j == n_kv - 1) {
+          // wait for the tile, zero the tail slots' rows in each 64-column box, make the
+          // writes visible to the tensor core, and release the tile to the MMA warps
+          if (!mbar_wait(vbar, j & 1, &sm.abort)) break;
+          const int r0 = Nk - j * BN, r1 = min(BN, ((Nk + 15) / 16) * 16 - j * BN);
+          for (int x = 0; x < D / 64; ++x)
+            for (int r = r0; r < r1; ++r)
+              for (int c = 0; c < 8; ++c) st_shared_v4(smem_u32(sm.v) + x * kBoxBytes + r * 128 + c * 16, 0, 0, 0, 0);
+          fence_proxy_async_smem();
+          mbar_arrive(smem_u32(&sm.v_tail));
+        }
         // V has one stage, so each tile's copy waits for the previous tile's P V:
         // start bringing the next tile into L2 now (dense and ragged layouts; for
         // the paged layout the extra page-id loads and per-page prefetches cost more
@@ -423,8 +441,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (j > 0) {
         const int jp = j - 1;
+        const bool tail = v_tail_fix && jp == n_kv - 1;  // the last tile, tail slots zeroed
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_full[c]), jp & 1, &sm.abort) &&
-                                         mbar_wait(smem_u32(&sm.v_full), jp & 1, &sm.abort));
+                                         (tail ? mbar_wait(smem_u32(&sm.v_tail), 0, &sm.abort)
+                                               : mbar_wait(smem_u32(&sm.v_full), jp & 1, &sm.abort)));
         if (!ok) break;
         tc05::fence_after_sync();
         if (elect_one()) {

@@ -170,9 +170,10 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
  *             bad page ids and kv_lens values beyond the table are handled the same way)
  *  qo_indptr  [B + 1] int32, device, checked as in attn_fwd_varlen (with total_q);
  *  max_q_len  as attn_fwd_varlen;  d in {64, 128}.
- * Each 128-key tile is loaded as whole 16-token pages, so the slots past
- * kv_lens[b] in a sequence's last page are read and multiplied by zero
- * weights: they must hold finite values (stale tokens or zeros, not NaN/Inf).
+ * Each 128-key tile is loaded as whole 16-token pages; the slots past
+ * kv_lens[b] in a sequence's last page may hold anything (stale tokens, NaN,
+ * Inf): their scores are masked and their V rows are zeroed in shared memory
+ * before P V, so they never reach O or the LSE.
  */
 attn_status_t attn_fwd_paged(const void *q, const void *k_pages, const void *v_pages, const int32_t *page_table,
                              const int32_t *kv_lens, const int32_t *qo_indptr, void *o, float *lse,
@@ -247,8 +248,9 @@ size_t attn_decode_workspace_size(int B, int H, int d, int max_splits);
  *  num_pages   P, the pool size (the tensor-map extent).  A page id outside [0, P)
  *              reads as zeros (TMA fills out-of-range boxes) and is recorded as
  *              ATTN_DEVERR_BAD_PAGE; so is a kv_lens value beyond the table.
- *              Slots past kv_lens[b] in a sequence's last page are read and
- *              weighted by zero: they must hold finite values.
+ *              Slots past kv_lens[b] in a sequence's last page may hold
+ *              anything (NaN and Inf included): their scores are masked and
+ *              their V rows zeroed in shared memory before P V.
  *  num_splits  upper bound on the key chunks per sequence; <= 0 picks one from
  *              B, Hkv, max_pages_per_seq and the SM count.  The chunk is
  *              ceil(max_pages_per_seq / num_splits) pages; sequence b uses

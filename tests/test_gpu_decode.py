@@ -118,3 +118,38 @@ def test_head_dim_64(cuda, H, Hkv, num_splits):
     check_o(o, O, torch.bfloat16, f"d=64 g={H // Hkv} splits={num_splits}")
     check_lse(lse, L, f"d=64 g={H // Hkv} splits={num_splits}")
     assert attn_device_error() == 0
+
+
+def poison_tail_slots(kv):
+    """Fill every slot past kv_lens[b] in each sequence's last page of K and V with NaN,
+    +Inf and -Inf (in turn), as a recycled or never-written page pool may hold."""
+    ps = kv.page_size
+    bad = torch.tensor([float("nan"), float("inf"), -float("inf")], dtype=torch.bfloat16)
+    n = 0
+    for b, L in enumerate(kv.kv_lens.tolist()):
+        if L % ps == 0:
+            continue
+        page = int(kv.page_table[b, L // ps])
+        for slot in range(L % ps, ps):
+            kv.k_pages[page, :, slot, :] = bad[n % 3]
+            kv.v_pages[page, :, slot, :] = bad[(n + 1) % 3]
+            n += 1
+    assert n > 0
+    return kv
+
+
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+@pytest.mark.parametrize("d", [64, 128])
+def test_non_finite_tail_slots_do_not_reach_the_output(cuda, d, num_splits):
+    """The slots of a last page past the sequence's length may hold anything: with NaN and
+    +-Inf there, O and the LSE still match the oracle (which reads only the first kv_lens[b]
+    tokens)."""
+    kv = poison_tail_slots(W.decode_inputs(8, 32, 8, d, 16, 1, 1, seed=41 + d,
+                                           kv_lens=[1, 15, 17, 33, 300, 1000, 2049, 5]))
+    attn_device_error(clear=True)
+    o, lse = run(kv, cuda, num_splits=num_splits)
+    O, L = ref(kv)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    check_o(o, O, torch.bfloat16, f"poisoned tails d={d} splits={num_splits}")
+    check_lse(lse, L, f"poisoned tails d={d} splits={num_splits}")
+    assert attn_device_error() == 0

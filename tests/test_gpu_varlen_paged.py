@@ -108,3 +108,27 @@ def test_varlen_bad_offsets_skip_the_sequence_and_set_the_error_bit(cuda):
     bad_kv[1] = 10 ** 6                               # keys of sequences 0 and 1 leave k
     attn_fwd_varlen(q.to(cuda), k.to(cuda), v.to(cuda), qo.to(cuda), bad_kv.to(cuda), 300, causal=True)
     assert attn_device_error(clear=True) & 0x8
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_paged_prefill_non_finite_tail_slots(cuda, d):
+    """NaN and +-Inf in the slots past each sequence's length (its last page's tail) do
+    not reach O or the LSE of the paged prefill."""
+    from tests.test_gpu_decode import poison_tail_slots
+    kv_lens = [17, 300, 1001, 2049, 5, 129]
+    q_lens = [17, 1, 128, 300, 5, 129]
+    kv = poison_tail_slots(W.decode_inputs(len(kv_lens), 8, 2, d, 16, 1, 1, seed=d + 7, kv_lens=kv_lens))
+    g = torch.Generator().manual_seed(d + 8)
+    q = torch.randn(sum(q_lens), 8, d, generator=g).to(torch.bfloat16)
+    qo = torch.tensor([0] + list(np.cumsum(q_lens)), dtype=torch.int32)
+    attn_device_error(clear=True)
+    for causal in (True, False):
+        o, lse = attn_fwd_paged(q.to(cuda), kv.k_pages.to(cuda), kv.v_pages.to(cuda), kv.page_table.to(cuda),
+                                kv.kv_lens.to(cuda), qo.to(cuda), max(q_lens), causal=causal)
+        torch.cuda.synchronize()
+        assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+        O, L = oracle.paged_prefill(q, kv.k_pages, kv.v_pages, kv.page_table, kv.kv_lens, qo, causal=causal,
+                                    scale=1 / math.sqrt(d))
+        check_o(o.cpu(), O, torch.bfloat16, f"paged prefill poisoned tails d={d} causal={causal}")
+        check_lse(lse.cpu(), L, f"paged prefill poisoned tails d={d} causal={causal}")
+    assert attn_device_error() == 0
