@@ -40,11 +40,13 @@
 //               maximum moves only when the row max outgrows it by more than
 //               2^8; the result does not depend on the reference, and p stays
 //               <= 256), and at the end write O = o~ / l and the LSE.
-//               The two warpgroups take turns for the exponentials (an mbarrier
-//               token: A's of tile j after B's of tile j-1, B's of tile j after
-//               A's of tile j), so that one chain's exponentials run while the
-//               other stores P and loads its next S, instead of both competing
-//               for the same sub-partitions' MUFU and issue slots at once.
+//               At d = 128 the two warpgroups take turns for the exponentials (an
+//               mbarrier token: A's of tile j after B's of tile j-1, B's of tile j
+//               after A's of tile j, passed on once the ex2 instructions are
+//               issued), so that one chain's exponentials run while the other packs
+//               and stores P and loads its next S, instead of both competing for the
+//               same sub-partitions' quarter-rate pipe at once.  At d = 64, with half
+//               the tensor work per exponential, they run without turns.
 // Tensor memory, 512 columns: S_A [0,128), S_B [128,256), O_A [256,256+d),
 // O_B [384,384+d).  At d = 64 the columns after each O hold that chain's P
 // (128 keys as 64 columns of packed bf16 pairs, written with tcgen05.st), and
@@ -177,6 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kRaggedK = kLay == kRagged;  // key offsets from kv_indptr (rows-outer K/V maps)
   constexpr bool kPagedK = kLay == kPaged;    // keys gathered page by page
   constexpr bool kPInTmem = D == 64;          // P_c kept in tensor memory for a TS-form P V
+  // The two softmax warpgroups take turns for their exponentials at d = 128; at d = 64 they
+  // run them concurrently (measured: +2 % with turns at d = 128, +7 % without them at d = 64).
+  constexpr bool kPingPong = D == 128;
   using Smem = PrefillSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -526,9 +531,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 1 when kept (also while the row has met no key at all); 0 on the row's first key
       const float corr = (m_next == m_ref) ? 1.f : ex2_approx(m_ref - m_next);
       m_ref = m_next;
-      // ping-pong: chain A's exponentials of tile j follow chain B's of tile j-1, and
-      // chain B's of tile j follow chain A's of tile j
-      {
+      // ping-pong (d = 128): chain A's exponentials of tile j follow chain B's of tile j-1,
+      // and chain B's of tile j follow chain A's of tile j
+      if (kPingPong) {
         const int need = c == 0 ? j - 1 : j;  // the other chain's step to wait for
         if (need >= 0 && need < n_tiles[1 - c] &&
             !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.turn[c]), need & 1, &sm.abort))) {
@@ -537,20 +542,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
-      // p = 2^(s * scale * log2(e) - m_ref), summed in eight partial sums, packed to bf16
-      // (a row that has met no key yet has every s = -inf and takes reference 0: p = 0)
+      // p = 2^(s * scale * log2(e) - m_ref), in place (a row that has met no key yet has
+      // every s = -inf and takes reference 0: p = 0).  The turn passes to the other chain
+      // as soon as the exponentials are issued: the bf16 packs below use the same
+      // quarter-rate pipe as ex2, and run while the other chain starts its exponentials.
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
       const uint64_t negm2 = f2(neg_m, neg_m);
-      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-      uint32_t pr[2][32];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float x0, x1;
           f2_split(fma2(f2(__uint_as_float(sr[q4][e]), __uint_as_float(sr[q4][e + 1])), scale2, negm2), x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
+          sr[q4][e] = __float_as_uint(ex2_approx(x0));
+          sr[q4][e + 1] = __float_as_uint(ex2_approx(x1));
+        }
+      }
+      if (kPingPong) mbar_arrive(smem_u32(&sm.turn[1 - c]));
+      // the row sum in eight partial sums, and P packed to bf16 (round to nearest even)
+      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+      uint32_t pr[2][32];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = __uint_as_float(sr[q4][e]), p1 = __uint_as_float(sr[q4][e + 1]);
           acc2[(e >> 1) & 3] = add2(acc2[(e >> 1) & 3], f2(p0, p1));
           pr[q4 >> 1][(q4 & 1) * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
         }
@@ -558,7 +574,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sum_lo, sum_hi;
       f2_split(add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3])), sum_lo, sum_hi);
       l = l * corr + (sum_lo + sum_hi);
-      mbar_arrive(smem_u32(&sm.turn[1 - c]));
 
       // P_c(j-1) V_{j-1} must have completed: it reads the P buffer written below
       // and o~ is rescaled in place
