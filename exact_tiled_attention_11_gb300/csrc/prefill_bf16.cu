@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const PrefillOut out, const PrefillLayout lay,
                         int B, int H, int Hkv, int Nq_max, int Nk_dense, int causal, float scale_log2,
-                        int q_rows_outer) {
+                        int q_rows_outer, int resident_ctas) {
   constexpr bool kRaggedQ = kLay != kDense;  // query rows are the outer dimension (q_plane = head)
   constexpr bool kIndptrQ = kLay == kRagged || kLay == kPaged;  // query offsets from qo_indptr
   constexpr bool kChunkK = kLay == kKeyChunks;  // batch b: keys [b * key_chunk, ...) of one shared set
@@ -250,43 +250,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // as zeros already (page id -1 lies outside the pool).
   const bool v_tail_fix = kPagedK && (Nk % 16) != 0 && n_kv > 0 && (n_kv - 1) * BN < Nk;
 
-  if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&sm.q_full), 1);
-    for (int s = 0; s < kKStages; ++s) {
-      mbar_init(smem_u32(&sm.k_full[s]), 1);
-      mbar_init(smem_u32(&sm.k_empty[0][s]), 1);
-      mbar_init(smem_u32(&sm.k_empty[1][s]), 1);
-    }
-    mbar_init(smem_u32(&sm.v_full), 1);
-    mbar_init(smem_u32(&sm.v_tail), 1);
-    mbar_init(smem_u32(&sm.v_empty[0]), 1);
-    mbar_init(smem_u32(&sm.v_empty[1]), 1);
-    for (int c = 0; c < 2; ++c) {
-      mbar_init(smem_u32(&sm.s_full[c]), 1);
-      mbar_init(smem_u32(&sm.s_free[c]), 128);
-      mbar_init(smem_u32(&sm.p_full[c]), 128);
-      mbar_init(smem_u32(&sm.pv_done[c]), 1);
-      mbar_init(smem_u32(&sm.turn[c]), 128);
-    }
-    mbar_init(smem_u32(&sm.mma_done[0]), 1);
-    mbar_init(smem_u32(&sm.mma_done[1]), 1);
-    sm.abort = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tc05::tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
-    tc05::tmem_relinquish();
-  }
-  tc05::fence_before_sync();
-  __syncthreads();
-  tc05::fence_after_sync();
-  const uint32_t tmem = sm.tmem_base;
-
-  // Register split: the CTA is launched with 384 threads x 168 registers =
-  // 64,512.  Warpgroup 0 (two TMA warps, two MMA warps) gives up to
-  // 56 per thread and the two softmax warpgroups take 224:
-  // 128 x 56 + 256 x 224 = 64,512, exactly the launch's allocation.
-  if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
   // Key tile j of this sequence into shared memory: one box per 64 columns, or,
   // paged, eight 16-token pages per 64 columns (a page id past the sequence or
   // outside the pool reads as zeros: TMA fills out-of-range boxes).
@@ -323,23 +286,84 @@ __global__ void __launch_bounds__(kThreads, 1)
       pages[pg] = id;
     }
   };
-  if (warp == 0) {
-    // ================================================================ TMA: Q and K
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      const uint64_t keep = l2_policy_evict_last();    // K tiles are re-read by other query tiles
-      const uint64_t once = l2_policy_evict_first();   // each Q tile is read once
-      const uint32_t qbar = smem_u32(&sm.q_full);
-      mbar_arrive_expect_tx(qbar, (has_b ? 2 : 1) * BM * D * 2);
-      for (int c = 0; c < (has_b ? 2 : 1); ++c)
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sm.q_full), 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(smem_u32(&sm.k_full[s]), 1);
+      mbar_init(smem_u32(&sm.k_empty[0][s]), 1);
+      mbar_init(smem_u32(&sm.k_empty[1][s]), 1);
+    }
+    mbar_init(smem_u32(&sm.v_full), 1);
+    mbar_init(smem_u32(&sm.v_tail), 1);
+    mbar_init(smem_u32(&sm.v_empty[0]), 1);
+    mbar_init(smem_u32(&sm.v_empty[1]), 1);
+    for (int c = 0; c < 2; ++c) {
+      mbar_init(smem_u32(&sm.s_full[c]), 1);
+      mbar_init(smem_u32(&sm.s_free[c]), 128);
+      mbar_init(smem_u32(&sm.p_full[c]), 128);
+      mbar_init(smem_u32(&sm.pv_done[c]), 1);
+      mbar_init(smem_u32(&sm.turn[c]), 128);
+    }
+    mbar_init(smem_u32(&sm.mma_done[0]), 1);
+    mbar_init(smem_u32(&sm.mma_done[1]), 1);
+    sm.abort = 0;
+    fence_barrier_init();
+    // Q, the first K tile and the first V tile at once, while tensor memory is allocated and
+    // the warps take their roles (the TMA warps' loops continue from tile 1)
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_first();
+    const uint32_t qbar = smem_u32(&sm.q_full);
+    mbar_arrive_expect_tx(qbar, (has_b ? 2 : 1) * BM * D * 2);
+    for (int c = 0; c < (has_b ? 2 : 1); ++c)
 #pragma unroll
-        for (int x = 0; x < D / 64; ++x)
-          // Q map dimensions: (d, rows, planes), or (d, planes, rows) when the query rows are the outer dimension
-          tma_load_3d_hint(smem_u32(sm.q[c]) + x * kBoxBytes, &tm_q, qbar, x * 64,
-                           q_rows_outer ? q_plane : q_base + row0[c], q_rows_outer ? q_base + row0[c] : q_plane, once);
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
+      for (int x = 0; x < D / 64; ++x)
+        tma_load_3d_hint(smem_u32(sm.q[c]) + x * kBoxBytes, &tm_q, qbar, x * 64,
+                         q_rows_outer ? q_plane : q_base + row0[c], q_rows_outer ? q_base + row0[c] : q_plane, once);
+    if (n_kv > 0) {
+      int pages[8];
+      tile_pages(0, pages);
+      mbar_arrive_expect_tx(smem_u32(&sm.k_full[0]), Smem::kTileBytes);
+      load_kv_tile(smem_u32(sm.k[0]), &tm_k, smem_u32(&sm.k_full[0]), 0, keep, pages);
+      mbar_arrive_expect_tx(smem_u32(&sm.v_full), Smem::kTileBytes);
+      load_kv_tile(smem_u32(sm.v), &tm_v, smem_u32(&sm.v_full), 0, keep, pages);
+    }
+  }
+  if (warp == 1) {
+    tc05::tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+    tc05::tmem_relinquish();
+  }
+  tc05::fence_before_sync();
+  __syncthreads();
+  tc05::fence_after_sync();
+  const uint32_t tmem = sm.tmem_base;
+
+  // Register split: the CTA is launched with 384 threads x 168 registers =
+  // 64,512.  Warpgroup 0 (two TMA warps, two MMA warps) gives up to
+  // 56 per thread and the two softmax warpgroups take 224:
+  // 128 x 56 + 256 x 224 = 64,512, exactly the launch's allocation.
+  if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+  if (warp == 0) {
+    // ================================================================ TMA: K (Q, K(0) issued above)
+    if (lane == 0) {
+      const uint64_t keep = l2_policy_evict_last();    // K tiles are re-read by other query tiles
+      const uint32_t qbar = smem_u32(&sm.q_full);
+      // The CTA that will probably run next on this SM (one CTA per SM, dispatched in grid
+      // order) needs its Q tiles first: bring them into L2 now (dense layout).
+      {
+        const int nb = blockIdx.x + resident_ctas;
+        if (!kRaggedQ && nb < static_cast<int>(gridDim.x)) {
+          const int nt = causal ? (n_pairs - 1 - nb / bh_count) : nb / bh_count;
+          const int nbh = nb % bh_count;
+          for (int c = 0; c < 2; ++c)
+            if ((2 * nt + c) * BM < Nq_max)
+#pragma unroll
+              for (int x = 0; x < D / 64; ++x) tma_prefetch_l2(&tm_q, x * 64, (2 * nt + c) * BM, nbh);
+        }
+      }
+      int issued = n_kv > 0 ? 1 : 0;  // Q and K(0) were issued at the start
+      for (int j = 1; j < n_kv; ++j) {
         const int ks = j % kKStages;
         int pages[8];
         tile_pages(j, pages);  // before the wait: the ids do not depend on the stage
@@ -363,48 +387,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 2) {
-    // ================================================================ TMA: V (single stage)
+    // ================================================================ TMA: V (single stage; V(0) issued above)
     if (lane == 0) {
-      tma_prefetch_desc(&tm_v);
       const uint64_t keep = l2_policy_evict_last();
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
+      const uint32_t vbar = smem_u32(&sm.v_full);
+      // paged layout, last tile: wait for it, zero the tail slots' rows in each 64-column box,
+      // make the writes visible to the tensor core, and release the tile to the MMA warps
+      auto zero_tail = [&](int j) {
+        if (!mbar_wait(vbar, j & 1, &sm.abort)) return false;
+        const int r0 = Nk - j * BN, r1 = min(BN, ((Nk + 15) / 16) * 16 - j * BN);
+        for (int x = 0; x < D / 64; ++x)
+          for (int r = r0; r < r1; ++r)
+            for (int c = 0; c < 8; ++c) st_shared_v4(smem_u32(sm.v) + x * kBoxBytes + r * 128 + c * 16, 0, 0, 0, 0);
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&sm.v_tail));
+        return true;
+      };
+      // V has one stage, so each tile's copy waits for the previous tile's P V: bring the
+      // next tile into L2 meanwhile (dense and ragged layouts; for the paged layout the
+      // extra page-id loads and per-page prefetches cost more than they save)
+      auto prefetch_l2 = [&](int j) {
+        if (kPagedK || j >= n_kv) return;
+#pragma unroll
+        for (int x = 0; x < D / 64; ++x) {
+          if (kRaggedK)
+            tma_prefetch_l2(&tm_v, x * 64, kv_plane, k_base + j * BN);
+          else
+            tma_prefetch_l2(&tm_v, x * 64, k_base + j * BN, kv_plane);
+        }
+      };
+      int issued = n_kv > 0 ? 1 : 0;
+      bool ok = !(v_tail_fix && n_kv == 1) || zero_tail(0);
+      prefetch_l2(1);
+      for (int j = 1; ok && j < n_kv; ++j) {
         int pages[8];
         tile_pages(j, pages);  // before the wait: the ids do not depend on the stage
-        bool free_ok = true;
-        for (int c = 0; c < 2 && free_ok; ++c)
-          if (j >= 1 && j - 1 < n_tiles[c]) free_ok = mbar_wait(smem_u32(&sm.v_empty[c]), (j - 1) & 1, &sm.abort);
-        if (!free_ok) break;
-        const uint32_t vbar = smem_u32(&sm.v_full);
+        for (int c = 0; c < 2 && ok; ++c)
+          if (j - 1 < n_tiles[c]) ok = mbar_wait(smem_u32(&sm.v_empty[c]), (j - 1) & 1, &sm.abort);
+        if (!ok) break;
         mbar_arrive_expect_tx(vbar, Smem::kTileBytes);
         load_kv_tile(smem_u32(sm.v), &tm_v, vbar, j, keep, pages);
         ++issued;
-        if (v_tail_fix && j == n_kv - 1) {
-          // wait for the tile, zero the tail slots' rows in each 64-column box, make the
-          // writes visible to the tensor core, and release the tile to the MMA warps
-          if (!mbar_wait(vbar, j & 1, &sm.abort)) break;
-          const int r0 = Nk - j * BN, r1 = min(BN, ((Nk + 15) / 16) * 16 - j * BN);
-          for (int x = 0; x < D / 64; ++x)
-            for (int r = r0; r < r1; ++r)
-              for (int c = 0; c < 8; ++c) st_shared_v4(smem_u32(sm.v) + x * kBoxBytes + r * 128 + c * 16, 0, 0, 0, 0);
-          fence_proxy_async_smem();
-          mbar_arrive(smem_u32(&sm.v_tail));
-        }
-        // V has one stage, so each tile's copy waits for the previous tile's P V:
-        // start bringing the next tile into L2 now (dense and ragged layouts; for
-        // the paged layout the extra page-id loads and per-page prefetches cost more
-        // than they save)
-        if (!kPagedK && j + 1 < n_kv) {
-#pragma unroll
-          for (int x = 0; x < D / 64; ++x) {
-            if (kRaggedK)
-              tma_prefetch_l2(&tm_v, x * 64, kv_plane, k_base + (j + 1) * BN);
-            else
-              tma_prefetch_l2(&tm_v, x * 64, k_base + (j + 1) * BN, kv_plane);
-          }
-        }
+        if (v_tail_fix && j == n_kv - 1) ok = zero_tail(j);
+        prefetch_l2(j + 1);
       }
-      if (issued > 0) mbar_wait(smem_u32(&sm.v_full), (issued - 1) & 1, nullptr);
+      if (issued > 0) mbar_wait(vbar, (issued - 1) & 1, nullptr);
     }
     __syncwarp();
   } else if (warp == 1 || warp == 3) {
@@ -670,9 +697,13 @@ cudaError_t launch_d(const PrefillMaps &maps, const PrefillOut &out, const Prefi
   const long long n_pairs = (Nq + 2 * BM - 1) / (2 * BM);
   const long long blocks = n_pairs * B * H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
   kern<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(maps.q, maps.k, maps.v, out, lay, B, H, Hkv, Nq,
                                                                    Nk, causal ? 1 : 0, scale * kLog2e,
-                                                                   maps.q_rows_outer ? 1 : 0);
+                                                                   maps.q_rows_outer ? 1 : 0, sms);
   return cudaGetLastError();
 }
 
