@@ -223,6 +223,39 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
 // attn_fwd_host: groups of (batch, KV head) planes in flight at once
 constexpr int kHostGroups = 4;
 
+// The events that order attn_fwd_host's three streams, created once per host thread and
+// device and reused by every call from that thread: a thread's calls are queued one after
+// another, and a stream wait binds to the event's latest record at the time it is queued.
+// They are released when the thread moves to another device, and otherwise kept until the
+// device's context goes away (no CUDA call from a thread-exit destructor, which may run
+// after the runtime has shut down).
+struct HostCallEvents {
+  int device = -1;
+  cudaEvent_t ev[2 + 2 * kHostGroups] = {};
+  void release() {
+    for (cudaEvent_t &e : ev)
+      if (e != nullptr) {
+        cudaEventDestroy(e);
+        e = nullptr;
+      }
+    device = -1;
+  }
+  // the events for the current device, or nullptr if they cannot be created
+  cudaEvent_t *get() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    if (dev == device) return ev;
+    release();
+    for (cudaEvent_t &e : ev)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+        release();
+        return nullptr;
+      }
+    device = dev;
+    return ev;
+  }
+};
+
 attn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void *v_host, void *o_host,
                             float *lse_host, void *q_dev, void *k_dev, void *v_dev, void *o_dev, float *lse_dev,
                             int B, int H, int Hkv, int N, int d, int causal, float scale, attn_dtype_t dtype,
@@ -249,15 +282,11 @@ attn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void *
   const size_t q_plane = kv_plane * g;                       // bytes of the plane's g query heads
   const size_t l_plane = static_cast<size_t>(N) * g * sizeof(float);
 
-  cudaEvent_t start, in_done[kHostGroups], fwd_done[kHostGroups], out_done;
-  bool created = true;
-  created &= cudaEventCreateWithFlags(&start, cudaEventDisableTiming) == cudaSuccess;
-  created &= cudaEventCreateWithFlags(&out_done, cudaEventDisableTiming) == cudaSuccess;
-  for (int i = 0; i < groups; ++i) {
-    created &= cudaEventCreateWithFlags(&in_done[i], cudaEventDisableTiming) == cudaSuccess;
-    created &= cudaEventCreateWithFlags(&fwd_done[i], cudaEventDisableTiming) == cudaSuccess;
-  }
-  if (!created) return ATTN_ERR_CUDA;
+  static thread_local HostCallEvents pool;
+  cudaEvent_t *ev = pool.get();
+  if (ev == nullptr) return ATTN_ERR_CUDA;
+  cudaEvent_t start = ev[0], out_done = ev[1];
+  cudaEvent_t *in_done = ev + 2, *fwd_done = ev + 2 + kHostGroups;
   attn_status_t status = ATTN_OK;
   auto check = [&](cudaError_t e) {
     if (e != cudaSuccess && status == ATTN_OK) status = ATTN_ERR_CUDA;
@@ -296,12 +325,6 @@ attn_status_t attn_fwd_host(const void *q_host, const void *k_host, const void *
   // `stream` covers everything the call queued
   check(cudaEventRecord(out_done, cout));
   check(cudaStreamWaitEvent(st, out_done, 0));
-  cudaEventDestroy(start);
-  cudaEventDestroy(out_done);
-  for (int i = 0; i < groups; ++i) {
-    cudaEventDestroy(in_done[i]);
-    cudaEventDestroy(fwd_done[i]);
-  }
   return status;
 }
 

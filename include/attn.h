@@ -91,8 +91,10 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
  * Group i: host-to-device copies of its Q, K, V rows on copy_in; attention of
  * the group on `stream` once they have landed; device-to-host copies of its O
  * and LSE rows on copy_out once that attention is done.  One cudaMemcpyAsync
- * per contiguous range; no memory is allocated (up to ten CUDA events are
- * created and released per call).
+ * per contiguous range; no memory is allocated.  The ten CUDA events that
+ * order the three streams are created on a thread's first call for a device
+ * and reused by its later calls (a thread's calls must not be captured into
+ * graphs that run concurrently with each other).
  *
  *  q_host, k_host, v_host, o_host, lse_host   host pointers, layouts and dtype as attn_fwd
  *             (lse_host may be NULL); page-locked memory is needed for the copies to
