@@ -10,14 +10,17 @@
 // head with one fp32 scale = amax / 448, and each value is stored as the e4m3
 // code of x / scale (round to nearest even, saturating).
 //
-// One CTA per (tensor, head plane, 128-row block), 512 threads: warp w holds
-// rows 8w .. 8w + 7 of the block, two rows per pass, sixteen lanes per row, lane l
-// columns 8 (l mod 16) .. + 7 (d = 128; one 16-byte load per lane and row).  The
-// Hadamard transform is the fast Walsh-Hadamard butterfly over the 7 bits of the
-// column index: bits 0-2 inside the lane (bits 1-2 on packed f32x2 pairs), bits 3-6
-// across the row's sixteen lanes with shuffles.  The 1/sqrt(d) normalisation does not change the codes
-// (the block's scale absorbs it), so it is only folded into the stored scale.
-// V is written transposed, v8t [plane, d, Nk_pad], so that both MMAs of the
+// One CTA per (tensor, head plane, 128-row block), 128 threads, thread t = row t of the
+// block.  The block's 32 KB of bf16 is contiguous in memory: it is staged in shared memory
+// with coalesced 16-byte cp.async copies (a 272-byte row pitch keeps both the staging
+// writes and each thread's row reads free of bank conflicts), each thread takes its row
+// into registers, applies the signs to the bf16 sign bits, and runs the whole 128-point
+// Walsh-Hadamard butterfly in registers: values are held as packed f32x2 pairs
+// (x[k], x[k + 64]), the stage on column bit 6 is the scalar first stage and the six
+// stages on bits 0..5 are packed add/sub between pairs k and k ^ 2^b.  The 1/sqrt(d)
+// normalisation does not change the codes (the block's scale absorbs it), so it is only
+// folded into the stored scale.  Codes are staged in shared memory and written out
+// coalesced.  V is written transposed, v8t [plane, d, Nk_pad], so that both MMAs of the
 // attention read K-major operands; keys in [Nk, Nk_pad) are zero.
 #include "common.cuh"
 #include "kernels.h"
@@ -27,8 +30,10 @@ namespace {
 
 constexpr int kRows = 128;
 constexpr int kD = 128;
-constexpr int kThreads = 512;
-constexpr int kRowsPerWarp = kRows / (kThreads / 32);
+constexpr int kThreads = 128;   // one per row
+constexpr int kInPitch = 272;   // bytes per staged bf16 row (256 + 16)
+constexpr int kOutPitch = 144;  // bytes per staged code row (128 + 16)
+constexpr int kVPitch = 132;    // bytes per staged V code row for the transposed copy-out
 constexpr float kE4m3Max = 448.f;
 
 // four fp32 values to four e4m3 codes (round to nearest even, saturating), a in the lowest byte
@@ -62,15 +67,27 @@ __device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 
-__global__ void __launch_bounds__(kThreads) fp8_quantize_kernel(Fp8QuantJob jq, Fp8QuantJob jk, Fp8QuantJob jv,
-                                                                 const float *signs, float transform_norm) {
-  __shared__ float warp_max[kThreads / 32];
-  __shared__ uint8_t tile[kRows][kD + 4];  // V codes; a 132-byte pitch keeps the column reads conflict-free
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int seg = lane & 15;      // this lane's columns: 8 seg .. 8 seg + 7
-  const int half = lane >> 4;     // which of the pass's two rows
+struct alignas(16) QuantSmem {
+  uint8_t rows[kRows * kInPitch];  // staged bf16 rows; later the codes (kOutPitch or kVPitch rows)
+  uint32_t sign_bits[kD / 2];      // per bf16 pair: the sign bits the transform's signs flip
+  float warp_max[kThreads / 32];
+};
+
+__global__ void __launch_bounds__(kThreads, 3) fp8_quantize_kernel(Fp8QuantJob jq, Fp8QuantJob jk, Fp8QuantJob jv,
+                                                                    const float *signs, float transform_norm) {
+  __shared__ QuantSmem sm;
+  const int t = threadIdx.x;
+  const int warp = t >> 5;
+  const int lane = t & 31;
 
   // ---- which tensor and block
   long long id = blockIdx.x;
@@ -92,104 +109,148 @@ __global__ void __launch_bounds__(kThreads) fp8_quantize_kernel(Fp8QuantJob jq, 
   const long long plane = id / nb;
   const int blk = static_cast<int>(id % nb);
   if (plane >= job.planes) return;
+  const int rows = min(kRows, job.N - blk * kRows);  // rows of this block inside the tensor
 
-  // ---- rows 8 warp + 2 p + half (p = 0..3), 8 columns each, times the signs; rows past N read as zero
-  float sg[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
-  if (transform) {
-    const float4 s0 = reinterpret_cast<const float4 *>(signs + seg * 8)[0];
-    const float4 s1 = reinterpret_cast<const float4 *>(signs + seg * 8)[1];
-    sg[0] = s0.x, sg[1] = s0.y, sg[2] = s0.z, sg[3] = s0.w, sg[4] = s1.x, sg[5] = s1.y, sg[6] = s1.z, sg[7] = s1.w;
+  // ---- stage the block: 16-byte chunk c = row c / 16, bytes 16 (c mod 16) .. + 15
+  const uint8_t *src = reinterpret_cast<const uint8_t *>(job.x + (plane * job.N + static_cast<long long>(blk) * kRows) * kD);
+  const uint32_t rows_s = smem_u32(sm.rows);
+#pragma unroll
+  for (int i = 0; i < kRows * kD * 2 / 16 / kThreads; ++i) {
+    const int c = t + i * kThreads;
+    if ((c >> 4) < rows) cp_async16(rows_s + (c >> 4) * kInPitch + (c & 15) * 16, src + c * 16);
   }
-  float x[kRowsPerWarp / 2][8];
+  if (transform && t < kD / 2)
+    sm.sign_bits[t] = (signs[2 * t] < 0.f ? 0x8000u : 0u) | (signs[2 * t + 1] < 0.f ? 0x80000000u : 0u);
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+
+  // ---- this row: x[k] and x[k + 64] as one packed pair, signs applied to the bf16 sign bits
+  uint64_t x[kD / 2];
+  {
+    uint32_t w[kD / 2];  // bf16 pairs (columns 2j, 2j + 1)
 #pragma unroll
-  for (int p = 0; p < kRowsPerWarp / 2; ++p) {
-    const int row = blk * kRows + warp * kRowsPerWarp + 2 * p + half;
-    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-    if (row < job.N) raw = reinterpret_cast<const uint4 *>(job.x + (plane * job.N + row) * kD)[seg];
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    for (int i = 0; i < kD / 8; ++i) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (t < rows) v = *reinterpret_cast<const uint4 *>(sm.rows + t * kInPitch + i * 16);
+      w[4 * i] = v.x, w[4 * i + 1] = v.y, w[4 * i + 2] = v.z, w[4 * i + 3] = v.w;
+    }
+    if (transform) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      x[p][2 * k] = __uint_as_float(w[k] << 16) * sg[2 * k];
-      x[p][2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u) * sg[2 * k + 1];
+      for (int i = 0; i < kD / 8; ++i) {
+        const uint4 m = reinterpret_cast<const uint4 *>(sm.sign_bits)[i];
+        w[4 * i] ^= m.x, w[4 * i + 1] ^= m.y, w[4 * i + 2] ^= m.z, w[4 * i + 3] ^= m.w;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kD / 2; ++k) {
+      // column k is the low or high half of word k / 2, column k + 64 of word 32 + k / 2
+      const uint32_t a = w[k >> 1], b = w[32 + (k >> 1)];
+      const float xa = __uint_as_float((k & 1) ? (a & 0xFFFF0000u) : (a << 16));
+      const float xb = __uint_as_float((k & 1) ? (b & 0xFFFF0000u) : (b << 16));
+      // column bit 6 first (scalar): (x[k], x[k + 64]) -> (x[k] + x[k + 64], x[k] - x[k + 64])
+      x[k] = transform ? f2(xa + xb, xa - xb) : f2(xa, xb);
     }
   }
-  // ---- x diag(signs) H_d: column bits 0..2 in the lane, bits 3..6 across the row's 16 lanes
   if (transform) {
+    // column bits 0..5: packed butterflies between pairs k and k ^ m
 #pragma unroll
-    for (int p = 0; p < kRowsPerWarp / 2; ++p) {
+    for (int m = 1; m < kD / 2; m <<= 1) {
 #pragma unroll
-      for (int i = 0; i < 8; i += 2) {  // bit 0
-        const float a = x[p][i], c = x[p][i + 1];
-        x[p][i] = a + c, x[p][i + 1] = a - c;
-      }
-#pragma unroll
-      for (int st = 2; st < 8; st <<= 1) {  // bits 1, 2 on packed pairs (i, i + 1)
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          if (i & st) continue;
-          const uint64_t lo = f2(x[p][i], x[p][i + 1]), hi = f2(x[p][i + st], x[p][i + st + 1]);
-          f2_split(add2(lo, hi), x[p][i], x[p][i + 1]);
-          f2_split(sub2(lo, hi), x[p][i + st], x[p][i + st + 1]);
-        }
-      }
-#pragma unroll
-      for (int m = 1; m < 16; m <<= 1) {  // bits 3..6: lanes seg ^ m of the same row
-        // lower lane: x + other, upper lane: other - x; fma with +-1 rounds exactly as the add
-        const float sgn = (seg & m) ? -1.f : 1.f;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) x[p][t] = fmaf(sgn, x[p][t], __shfl_xor_sync(0xffffffffu, x[p][t], m));
+      for (int k = 0; k < kD / 2; ++k) {
+        if (k & m) continue;
+        const uint64_t lo = x[k], hi = x[k | m];
+        x[k] = add2(lo, hi);
+        x[k | m] = sub2(lo, hi);
       }
     }
   }
   // ---- block amax
   float amax = 0.f;
 #pragma unroll
-  for (int p = 0; p < kRowsPerWarp / 2; ++p)
-#pragma unroll
-    for (int t = 0; t < 8; ++t) amax = fmaxf(amax, fabsf(x[p][t]));
+  for (int k = 0; k < kD / 2; ++k) {
+    float a, b;
+    f2_split(x[k], a, b);
+    amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
+  }
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-  if (lane == 0) warp_max[warp] = amax;
-  __syncthreads();
-  amax = warp_max[0];
-#pragma unroll
-  for (int w = 1; w < kThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
+  if (lane == 0) sm.warp_max[warp] = amax;
+  __syncthreads();  // also: every row has been read out of the staging buffer
+  amax = fmaxf(fmaxf(sm.warp_max[0], sm.warp_max[1]), fmaxf(sm.warp_max[2], sm.warp_max[3]));
   const float inv = amax > 0.f ? kE4m3Max / amax : 0.f;
-  if (threadIdx.x == 0) job.scale[plane * nb + blk] = amax / kE4m3Max * (transform ? transform_norm : 1.f);
+  if (t == 0) job.scale[plane * nb + blk] = amax / kE4m3Max * (transform ? transform_norm : 1.f);
 
-  // ---- codes: 8 bytes per lane and row
+  // ---- codes of this row: columns 16 i .. 16 i + 15 -> one 16-byte word
+  const uint64_t inv2 = f2(inv, inv);
+  const int pitch = transposed ? kVPitch : kOutPitch;
 #pragma unroll
-  for (int p = 0; p < kRowsPerWarp / 2; ++p) {
-    const int row_in = warp * kRowsPerWarp + 2 * p + half;
-    const int row = blk * kRows + row_in;
-    const uint32_t c0 = pack_e4m3x4(x[p][0] * inv, x[p][1] * inv, x[p][2] * inv, x[p][3] * inv);
-    const uint32_t c1 = pack_e4m3x4(x[p][4] * inv, x[p][5] * inv, x[p][6] * inv, x[p][7] * inv);
-    if (!transposed) {
-      if (row < job.N) reinterpret_cast<uint2 *>(job.out + (plane * job.N + row) * kD)[seg] = make_uint2(c0, c1);
+  for (int i = 0; i < kD / 16; ++i) {
+    uint32_t c[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      // columns 16 i + 4 q .. + 3: the low (i < 4) or high (i >= 4) halves of pairs (16 i + 4 q) mod 64 ..
+      const int k0 = (16 * i + 4 * q) & 63;
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float lo, hi;
+        f2_split(mul2(x[k0 + e], inv2), lo, hi);
+        v[e] = i < 4 ? lo : hi;
+      }
+      c[q] = pack_e4m3x4(v[0], v[1], v[2], v[3]);
+    }
+    uint8_t *dst = sm.rows + t * pitch + i * 16;
+    if (transposed) {  // 4-byte aligned rows (the 132-byte pitch)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) reinterpret_cast<uint32_t *>(dst)[q] = c[q];
     } else {
-      uint32_t *t = reinterpret_cast<uint32_t *>(&tile[row_in][8 * seg]);
-      t[0] = c0;
-      t[1] = c1;
+      *reinterpret_cast<uint4 *>(dst) = make_uint4(c[0], c[1], c[2], c[3]);
     }
   }
-  if (!transposed) return;
   __syncthreads();
-  // ---- V^T: row dd of the plane holds the block's keys; 16 keys (one 16-byte store) per step
+
+  if (!transposed) {
+    // ---- row-major codes, coalesced: chunk c = row c / 8, bytes 16 (c mod 8) .. + 15
+    uint8_t *dst = job.out + (plane * job.N + static_cast<long long>(blk) * kRows) * kD;
+#pragma unroll
+    for (int i = 0; i < kRows * kD / 16 / kThreads; ++i) {
+      const int c = t + i * kThreads;
+      if ((c >> 3) < rows)
+        *reinterpret_cast<uint4 *>(dst + c * 16) =
+            *reinterpret_cast<const uint4 *>(sm.rows + (c >> 3) * kOutPitch + (c & 7) * 16);
+    }
+    return;
+  }
+  // ---- V^T: row dd of the plane holds the block's keys.  Warp w takes key groups kc = w, w + 4
+  // (16 keys each) and lane l dims 4 l .. 4 l + 3: 32-bit reads of four keys' four codes
+  // (conflict-free: the 132-byte pitch puts the 32 lanes' words in 32 banks), a 4 x 4 byte
+  // transpose in registers, one 16-byte store of 16 keys per dim.
   const int n_pad = job.n_pad;
 #pragma unroll
-  for (int i = 0; i < (kD * kRows / 16) / kThreads; ++i) {
-    const int chunk = threadIdx.x + i * kThreads;
-    const int dd = chunk / (kRows / 16);
-    const int kc = chunk % (kRows / 16);
+  for (int g = 0; g < kRows / 16 / (kThreads / 32); ++g) {
+    const int kc = warp + g * (kThreads / 32);
     const int key0 = blk * kRows + kc * 16;
-    if (key0 >= n_pad) continue;
-    uint32_t w[4];
+    if (key0 >= n_pad) continue;  // warp-uniform
+    uint32_t col[4][4];  // [dim j][4-key group]: keys 4 group .. + 3 of dim 4 lane + j
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      w[q] = static_cast<uint32_t>(tile[kc * 16 + 4 * q][dd]) | (static_cast<uint32_t>(tile[kc * 16 + 4 * q + 1][dd]) << 8) |
-             (static_cast<uint32_t>(tile[kc * 16 + 4 * q + 2][dd]) << 16) |
-             (static_cast<uint32_t>(tile[kc * 16 + 4 * q + 3][dd]) << 24);
-    *reinterpret_cast<uint4 *>(job.out + (plane * kD + dd) * n_pad + key0) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int q = 0; q < 4; ++q) {
+      // keys past N (a partial last block) were quantised from zeros: zero codes
+      const uint8_t *p = sm.rows + (kc * 16 + 4 * q) * kVPitch + 4 * lane;
+      const uint32_t r0 = *reinterpret_cast<const uint32_t *>(p);
+      const uint32_t r1 = *reinterpret_cast<const uint32_t *>(p + kVPitch);
+      const uint32_t r2 = *reinterpret_cast<const uint32_t *>(p + 2 * kVPitch);
+      const uint32_t r3 = *reinterpret_cast<const uint32_t *>(p + 3 * kVPitch);
+      const uint32_t t0 = __byte_perm(r0, r1, 0x5140), t1 = __byte_perm(r0, r1, 0x7362);
+      const uint32_t t2 = __byte_perm(r2, r3, 0x5140), t3 = __byte_perm(r2, r3, 0x7362);
+      col[0][q] = __byte_perm(t0, t2, 0x5410);
+      col[1][q] = __byte_perm(t0, t2, 0x7632);
+      col[2][q] = __byte_perm(t1, t3, 0x5410);
+      col[3][q] = __byte_perm(t1, t3, 0x7632);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint4 *>(job.out + (plane * kD + 4 * lane + j) * n_pad + key0) =
+          make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
   }
 }
 
