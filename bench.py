@@ -212,7 +212,7 @@ def fp8_variant(dev, d, t_peak, hbm_peak, reps=10):
     """attn_fp8_quantize + attn_fwd_fp8 on the benchmark's prefill inputs (B=1, H=32,
     Hkv=8, N=8192, d=128, causal), timed apart from the step: each launch between
     its own pair of CUDA events, with a 256 MiB write between launches so that no
-    input is served from L2.  The fp8 tensor peak is the measured bf16 peak times
+    input is served from L2 and a device delay after it (device time only).  The fp8 tensor peak is the measured bf16 peak times
     the nominal fp8/bf16 ratio (2)."""
     import torch
     import exact_tiled_attention_11_gb300 as lib
@@ -230,6 +230,7 @@ def fp8_variant(dev, d, t_peak, hbm_peak, reps=10):
         tot = 0.0
         for _ in range(reps):
             flush.fill_(1)
+            device_delay(stream, 100.0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             fn()
@@ -310,16 +311,27 @@ def launch_overhead(dev, calls=20, reps=20):
 
 # ------------------------------------------------------------------ every workload, timed alone
 
+def device_delay(stream, us):
+    """Keep ``stream`` busy for about ``us`` microseconds with a spin kernel, so that the
+    work queued behind it is already enqueued when it ends: an event-timed region that
+    starts after it measures device time, not the host's time to enqueue the launch
+    (host costs are in the end-to-end measurement)."""
+    import torch
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(us * 2.1e3))  # cycles at up to 2.1 GHz
+
+
 def time_launches(stream, fn, flush, reps, warmup=5):
     """Event-timed launches of ``fn`` on ``stream``: each between its own pair of CUDA
-    events, an L2-sized write between launches (outside the events).  Returns the
-    sorted per-launch milliseconds."""
+    events, an L2-sized write and a 100 us device delay between launches (outside the
+    events).  Returns the sorted per-launch milliseconds."""
     import torch
     for _ in range(warmup):
         fn()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
     for e0, e1 in ev:
         flush.fill_(1)
+        device_delay(stream, 100.0)
         e0.record(stream)
         fn()
         e1.record(stream)
@@ -600,6 +612,8 @@ def run_ours(args, rank, local_rank, world):
         start = torch.cuda.Event(enable_timing=True)
         stop = torch.cuda.Event(enable_timing=True)
         lib.attn_clock_probe(probe[:4], stream=stream)
+        # the first step's launches are enqueued while this delay runs (device time only)
+        device_delay(stream, 300.0)
         start.record(stream)
         for i in range(args.steps):
             ev[i][0].record(stream)

@@ -636,7 +636,9 @@ attn_status_t attn_clock_probe(uint64_t *out, const uint64_t *match, attn_stream
   if (out == nullptr || (reinterpret_cast<uintptr_t>(out) & 7u) != 0 ||
       (match != nullptr && (reinterpret_cast<uintptr_t>(match) & 7u) != 0))
     return ATTN_ERR_INVALID_ARG;
-  const int blocks = 16 * std::max(device_sm_count(), 1);  // every SM gets blocks
+  // without `match` one block records on whichever SM runs it; with `match`, every SM gets
+  // blocks so that one of them runs on the recorded SM (the others return at once)
+  const int blocks = match == nullptr ? 1 : 16 * std::max(device_sm_count(), 1);
   return attn::launch_clock_probe(reinterpret_cast<unsigned long long *>(out),
                                   reinterpret_cast<const unsigned long long *>(match), blocks,
                                   reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess

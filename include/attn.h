@@ -407,8 +407,9 @@ attn_status_t attn_selftest_wait_timeout(int32_t *gave_up, attn_stream_t stream)
  *   out    [4] uint64, device, 8-byte aligned: {global timer ns, clock64, SM id, claim};
  *          zeroed by the call, then written by the first probe block on the chosen SM
  *          (claim = 1 once written; 0 means no block ran there)
- *   match  NULL: any SM; or an earlier probe's `out` (read on the device when this
- *          probe runs): record on the same SM, since clock64 is a per-SM counter
+ *   match  NULL: any SM (one block); or an earlier probe's `out` (read on the device
+ *          when this probe runs): record on the same SM, since clock64 is a per-SM
+ *          counter (blocks on every SM; those on other SMs return at once)
  * Two probes around work on one stream give its average SM clock in MHz:
  * 1000 * (clock64 difference) / (timer difference).  Returns ATTN_ERR_INVALID_ARG
  * for a null or misaligned pointer, ATTN_ERR_CUDA if the launch failed.
