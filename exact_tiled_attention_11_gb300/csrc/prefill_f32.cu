@@ -30,7 +30,6 @@
 namespace attn {
 namespace {
 
-constexpr int kSplits = 4;      // warps per CTA; each takes every kSplits-th key tile of the row
 constexpr int kTile = 32;       // keys per tile (one per lane)
 
 // error-free transformations (exact: a + b = s + err, a * b = p + err)
@@ -60,20 +59,34 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_b
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Per head dimension: the warps per CTA (each takes every kSplits-th key tile of the row) and
+// where a tile's V lives.  At d = 64 each lane holds its two columns of the tile's 32 V rows
+// in registers (64 values, read with coalesced loads while K is staged), so that only K
+// takes shared memory and eight warps still leave room for several CTAs per SM (a 256-key
+// row is then one tile per warp); at d = 128 V is staged in shared memory beside K.
+template <int D>
+struct F32Cfg {
+  static constexpr int kSplits = D == 64 ? 8 : 4;
+  static constexpr bool kVRegs = D == 64;
+};
+
 template <int D>
 struct F32Smem {
+  static constexpr int kSplits = F32Cfg<D>::kSplits;
   static constexpr int kStride = D + 4;   // padded K row: float4 reads of 8 lanes hit 8 distinct bank groups
   float k[kSplits][kTile * kStride];      // each warp's own key tile (lane j reads key j)
-  float v[kSplits][kTile * D];            // each warp's own value tile (lanes read along d)
+  float v[F32Cfg<D>::kVRegs ? 1 : kSplits][F32Cfg<D>::kVRegs ? 4 : kTile * D];  // each warp's value tile
   float q[D];
 };
 
 template <int D>
-__global__ void __launch_bounds__(kSplits * 32)
+__global__ void __launch_bounds__(F32Cfg<D>::kSplits * 32)
     prefill_f32_kernel(const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
                        PrefillOut out, int H, int Hkv, int Nq, int Nk, int causal, float scale) {
   constexpr int E = D / 32;                // output elements per lane
   constexpr int kStride = F32Smem<D>::kStride;
+  constexpr int kSplits = F32Cfg<D>::kSplits;
+  constexpr bool kVRegs = F32Cfg<D>::kVRegs;
   extern __shared__ float4 smem_f4[];
   F32Smem<D> &sm = *reinterpret_cast<F32Smem<D> *>(smem_f4);
 
@@ -93,7 +106,8 @@ __global__ void __launch_bounds__(kSplits * 32)
   for (int e = 4 * threadIdx.x; e < D; e += 4 * kSplits * 32) cp_async16(sm.q + e, qh + e, 16);
 
   float *ks = sm.k[warp];
-  float *vs = sm.v[warp];
+  float *vs = sm.v[kVRegs ? 0 : warp];
+  float vr[kVRegs ? kTile : 1][E];         // d = 64: lane's columns lane + 32 j of the tile's V rows
   float m = -INFINITY;                     // running max of s_hi (warp-uniform)
   float l_hi = 0.f, l_lo = 0.f;            // row sum over this warp's keys (warp-uniform)
   float acc_hi[E], acc_lo[E];              // o~ elements lane + 32 j
@@ -110,7 +124,16 @@ __global__ void __launch_bounds__(kSplits * 32)
       const bool in = t0 + r < key_end;
       const size_t off = in ? static_cast<size_t>(t0 + r) * D + c : 0;
       cp_async16(ks + r * kStride + c, kh + off, in ? 16 : 0);
-      cp_async16(vs + r * D + c, vh + off, in ? 16 : 0);
+      if (!kVRegs) cp_async16(vs + r * D + c, vh + off, in ? 16 : 0);
+    }
+    if (kVRegs) {  // rows past key_end read as zeros (their p is 0)
+#pragma unroll
+      for (int jj = 0; jj < (kVRegs ? kTile : 0); ++jj) {
+        const bool in = t0 + jj < key_end;
+#pragma unroll
+        for (int j = 0; j < E; ++j)
+          vr[jj][j] = in ? __ldg(vh + static_cast<size_t>(t0 + jj) * D + lane + 32 * j) : 0.f;
+      }
     }
     const int t_next = t0 + kSplits * kTile;
     if (t_next + lane < key_end) {
@@ -195,11 +218,21 @@ __global__ void __launch_bounds__(kSplits * 32)
     float tile[E];
 #pragma unroll
     for (int j = 0; j < E; ++j) tile[j] = 0.f;
-    const int n_keys = min(kTile, key_end - t0);
-    for (int jj = 0; jj < n_keys; ++jj) {
-      const float pj = __shfl_sync(0xffffffffu, p, jj);
+    if (kVRegs) {
+      // keys past key_end contribute p = 0 times v = 0: the sum is unchanged
 #pragma unroll
-      for (int j = 0; j < E; ++j) tile[j] = fmaf(pj, vs[jj * D + lane + 32 * j], tile[j]);
+      for (int jj = 0; jj < (kVRegs ? kTile : 0); ++jj) {
+        const float pj = __shfl_sync(0xffffffffu, p, jj);
+#pragma unroll
+        for (int j = 0; j < E; ++j) tile[j] = fmaf(pj, vr[jj][j], tile[j]);
+      }
+    } else {
+      const int n_keys = min(kTile, key_end - t0);
+      for (int jj = 0; jj < n_keys; ++jj) {
+        const float pj = __shfl_sync(0xffffffffu, p, jj);
+#pragma unroll
+        for (int j = 0; j < E; ++j) tile[j] = fmaf(pj, vs[jj * D + lane + 32 * j], tile[j]);
+      }
     }
 #pragma unroll
     for (int j = 0; j < E; ++j) {
@@ -255,6 +288,7 @@ __global__ void __launch_bounds__(kSplits * 32)
 template <int D>
 cudaError_t launch_d(const float *q, const float *k, const float *v, const PrefillOut &out, int B, int H, int Hkv,
                      int Nq, int Nk, bool causal, float scale, cudaStream_t stream) {
+  constexpr int kSplits = F32Cfg<D>::kSplits;
   const size_t smem = sizeof(F32Smem<D>);
   auto kern = prefill_f32_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
