@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const PrefillOut out, const PrefillLayout lay,
                         int B, int H, int Hkv, int Nq_max, int Nk_dense, int causal, float scale_log2,
-                        int q_rows_outer, int resident_ctas, int n_items) {
+                        int q_rows_outer, int resident_ctas, int n_items, int plane_group) {
   constexpr bool kRaggedQ = kLay != kDense;  // query rows are the outer dimension (q_plane = head)
   constexpr bool kIndptrQ = kLay == kRagged || kLay == kPaged;  // query offsets from qo_indptr
   constexpr bool kChunkK = kLay == kKeyChunks;  // batch b: keys [b * key_chunk, ...) of one shared set
@@ -211,7 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int idx = k * G + ((k & 1) ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
     return idx < n_items ? idx : -1;
   };
-  // Item idx: pair t of (batch, head) bh, heaviest causal pairs first.  A sequence whose
+  // Item idx: pair t of (batch, head) bh, heaviest causal pairs first, over all planes or,
+  // with plane_group > 0, over groups of that many consecutive planes in turn (so that the
+  // CTAs running at once read the K and V of one group, which fits in L2).  A sequence whose
   // offsets leave [0, total) or exceed the host's max_q_len is not computed (its rows stay
   // unwritten) and sets BAD_LENGTH.  Every thread computes the same values.
   auto make_item = [&](int idx, bool record) {
@@ -222,8 +224,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       it.has_b = it.v_tail_fix = it.valid = false;
       return it;
     }
-    const int rank = idx / bh_count;
-    const int bh = idx % bh_count;
+    int rank, bh;
+    if (plane_group > 0 && plane_group < bh_count) {
+      const int per_group = plane_group * n_pairs;
+      const int g = idx / per_group, r = idx - g * per_group;
+      const int in_group = min(plane_group, bh_count - g * plane_group);  // the last group may be smaller
+      rank = r / in_group;
+      bh = g * plane_group + r % in_group;
+    } else {
+      rank = idx / bh_count;
+      bh = idx % bh_count;
+    }
     it.t = causal ? (n_pairs - 1 - rank) : rank;
     it.b = bh / H;
     it.h = bh % H;
@@ -808,7 +819,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, int kLay, bool kPersistent>
 cudaError_t launch_d(const PrefillMaps &maps, const PrefillOut &out, const PrefillLayout &lay, int B, int H, int Hkv,
-                     int Nq, int Nk, bool causal, float scale, long long items, int sms, cudaStream_t stream) {
+                     int Nq, int Nk, bool causal, float scale, long long items, int sms, cudaStream_t stream,
+                     int plane_group = 0) {
   // One CTA per SM: the kernel holds all 512 tensor-memory columns.
   const size_t smem = std::max<size_t>(sizeof(PrefillSmem<D>) + 1024, 120 * 1024);
   auto kern = prefill_bf16_kernel<D, kLay, kPersistent>;
@@ -818,7 +830,7 @@ cudaError_t launch_d(const PrefillMaps &maps, const PrefillOut &out, const Prefi
   kern<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(maps.q, maps.k, maps.v, out, lay, B, H, Hkv, Nq,
                                                                    Nk, causal ? 1 : 0, scale * kLog2e,
                                                                    maps.q_rows_outer ? 1 : 0, sms,
-                                                                   static_cast<int>(items));
+                                                                   static_cast<int>(items), plane_group);
   return cudaGetLastError();
 }
 
@@ -847,7 +859,20 @@ cudaError_t launch_layout(const PrefillMaps &maps, const PrefillOut &out, const 
   const long long avg_tiles = causal ? (kt + 1) / 2 : kt;
   if (items >= 4LL * sms && avg_tiles <= 48)
     return launch_d<D, kDense, true>(maps, out, lay, B, H, Hkv, Nq, Nk, causal, scale, items, sms, stream);
-  return launch_d<D, kDense, false>(maps, out, lay, B, H, Hkv, Nq, Nk, causal, scale, items, sms, stream);
+  // One item per CTA, heaviest first: the CTAs running at once take the same pairs of every
+  // (batch, head) plane.  When all planes' K and V exceed half of L2, take the planes in
+  // groups whose K and V fit there (whole GQA groups), so that K and V are read from DRAM
+  // about once instead of once per few query-tile pairs.
+  int l2 = 0;
+  if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) l2 = 0;
+  const long long kv_plane_bytes = static_cast<long long>(Nk) * D * 2 * 2;  // K and V of one KV head
+  int plane_group = 0;
+  if (l2 > 0 && kv_plane_bytes * B * Hkv > l2 / 2) {
+    const long long kv_planes = std::max<long long>(1, (l2 / 2) / std::max<long long>(kv_plane_bytes, 1));
+    plane_group = static_cast<int>(std::min<long long>(kv_planes * (H / Hkv), static_cast<long long>(B) * H));
+  }
+  return launch_d<D, kDense, false>(maps, out, lay, B, H, Hkv, Nq, Nk, causal, scale, items, sms, stream,
+                                    plane_group);
 }
 
 }  // namespace
