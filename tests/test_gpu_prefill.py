@@ -130,6 +130,24 @@ def test_c5_full_size_sampled(cuda, q_mult):
     _check_sampled(cfg, q, k, v, o, lse, heads=[0, 9, 15], tag=f"C5 x{q_mult}")
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_grouped_planes_gqa_sampled(cuda, causal):
+    """One CTA per query-tile pair with all planes' K and V beyond half of L2 (67 MB here): on
+    GB300 the launcher takes the query heads in groups of whole GQA groups whose K and V fit
+    in half of L2 (28 heads = 7 KV heads, then a last group of 4).  Sampled rows of heads in
+    both groups and on both sides of the boundary against the oracle."""
+    cfg = W.PrefillConfig("gqa_b1_h32_hkv8_n16384_d128", 1, 32, 8, 16384, 128, "bf16", (causal,))
+    q, k, v = W.prefill_inputs_for(cfg, seed=3)
+    o, lse = run(q, k, v, causal, cfg.scale, cuda)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    rng = np.random.default_rng(23)
+    for h in (0, 13, 27, 28, 31):
+        rows = _sampled_rows(cfg.N, rng)
+        O, L = oracle.attention_rows(q, k, v, 0, h, rows, causal=causal, scale=cfg.scale)
+        check_o(o[0, h, rows], O, torch.bfloat16, f"grouped GQA h{h} causal={causal}")
+        check_lse(lse[0, h, rows], L, f"grouped GQA h{h} causal={causal}")
+
+
 # ---------------------------------------------------------------- the pages' worked examples on the GPU
 
 def _p4_inputs(d, dtype):
