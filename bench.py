@@ -317,8 +317,11 @@ def device_delay(stream, us):
     starts after it measures device time, not the host's time to enqueue the launch
     (host costs are in the end-to-end measurement)."""
     import torch
+    sleep = getattr(torch.cuda, "_sleep", None)  # PyTorch's spin kernel (clock cycles)
+    if sleep is None:
+        return
     with torch.cuda.stream(stream):
-        torch.cuda._sleep(int(us * 2.1e3))  # cycles at up to 2.1 GHz
+        sleep(int(us * 2.1e3))  # cycles at up to 2.1 GHz
 
 
 def time_launches(stream, fn, flush, reps, warmup=5):
