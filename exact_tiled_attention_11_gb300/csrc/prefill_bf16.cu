@@ -94,6 +94,8 @@ struct PrefillSmem {
   uint64_t mma_done[2];
   uint32_t tmem_base;
   int abort;
+  // one item per CTA at d = 128: the first 64-key box of P_c is in shared memory
+  alignas(8) uint64_t p_half[2];
 };
 
 // ---- packed fp32 pairs (Blackwell f32x2 ALU forms)
@@ -187,6 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kRaggedK = kLay == kRagged;  // key offsets from kv_indptr (rows-outer K/V maps)
   constexpr bool kPagedK = kLay == kPaged;    // keys gathered page by page
   constexpr bool kPInTmem = D == 64;          // P_c kept in tensor memory for a TS-form P V
+  // P_c through shared memory in two 64-key boxes, each with its own ready barrier, so that
+  // P V starts on the first box while the second is stored (one item per CTA only)
+  constexpr bool kSplitP = !kPInTmem && !kPersistent;
   // Persistent form (dense layout, chosen by the host for many short items): each CTA takes
   // items blockIdx.x, 2G-1-blockIdx.x, 2G+blockIdx.x, ... (G CTAs, a snake over the
   // heaviest-first item order), so that one item's Q and first tiles load and its first
@@ -367,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.s_full[c]), 1);
       mbar_init(smem_u32(&sm.s_free[c]), 128);
       mbar_init(smem_u32(&sm.p_full[c]), 128);
+      if (kSplitP) mbar_init(smem_u32(&sm.p_half[c]), 128);
       mbar_init(smem_u32(&sm.pv_done[c]), 1);
       mbar_init(smem_u32(&sm.turn[c]), 128);
     }
@@ -588,14 +594,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j > 0) {
           const int jp = j - 1;
           const bool tail = it.v_tail_fix && jp == it.n_kv - 1;  // the last tile, tail slots zeroed
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_full[c]), (ts + jp) & 1, &sm.abort) &&
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(kSplitP ? &sm.p_half[c] : &sm.p_full[c]), (ts + jp) & 1, &sm.abort) &&
                                            (tail ? mbar_wait(smem_u32(&sm.v_tail), 0, &sm.abort)
                                                  : mbar_wait(smem_u32(&sm.v_full), (gk + jp) & 1, &sm.abort)));
           if (!ok) break;
           tc05::fence_after_sync();
           if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
+            for (int kk = 0; kk < (kSplitP ? BN / 32 : BN / 16); ++kk) {
               if (kPInTmem)  // P_c in tensor memory beside O_c: 16 keys = 8 columns of packed bf16 pairs
                 tc05::mma_ts(tmem + 2 * BN + c * BN, tmem + 2 * BN + c * BN + D + kk * 8,
                              tc05::sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_pv, (jp > 0) || (kk > 0));
@@ -604,6 +610,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                              tc05::sdesc_sw128(p_addr + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
                              tc05::sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_pv, (jp > 0) || (kk > 0));
             }
+          }
+          __syncwarp();
+          if (kSplitP) {  // the second 64-key box of P
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_full[c]), (ts + jp) & 1, &sm.abort)))) break;
+            tc05::fence_after_sync();
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = BN / 32; kk < BN / 16; ++kk)
+                tc05::mma_ss(tmem + 2 * BN + c * BN,
+                             tc05::sdesc_sw128(p_addr + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+                             tc05::sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_pv, true);
+            }
+            __syncwarp();
+          }
+          if (elect_one()) {
             tc05::commit(smem_u32(&sm.pv_done[c]));
             tc05::commit(smem_u32(&sm.v_empty[c]));
           }
@@ -752,12 +773,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           // P row -> shared memory: keys 64x + 8ch .. +7 at chunk ch of box x, chunk index XOR (row mod 8)
 #pragma unroll
-          for (int x = 0; x < 2; ++x)
+          for (int x = 0; x < 2; ++x) {
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
               st_shared_v4(p_row + x * kBoxBytes + (((ch ^ row) & 7) << 4), pr[x][4 * ch], pr[x][4 * ch + 1],
                            pr[x][4 * ch + 2], pr[x][4 * ch + 3]);
-          fence_proxy_async_smem();
+            if (kSplitP) {  // P V may start on the first 64 keys
+              fence_proxy_async_smem();
+              if (x == 0) mbar_arrive(smem_u32(&sm.p_half[c]));
+            }
+          }
+          if (!kSplitP) fence_proxy_async_smem();
         }
         tc05::tmem_wait_st();
         tc05::fence_before_sync();
