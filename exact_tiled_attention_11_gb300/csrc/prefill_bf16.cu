@@ -878,15 +878,19 @@ cudaError_t launch_layout(const PrefillMaps &maps, const PrefillOut &out, const 
     return launch_d<D, kPaged, false>(maps, out, lay, B, H, Hkv, Nq, Nk, causal, scale, items, sms, stream);
   if (lay.kv_indptr != nullptr)
     return launch_d<D, kRagged, false>(maps, out, lay, B, H, Hkv, Nq, Nk, causal, scale, items, sms, stream);
-  // Dense: the persistent form pays when items are many (at least four per SM) and short (at
-  // most 48 key tiles on average): then the ~2.5 tiles' worth of set-up, first loads and
-  // epilogue per item that it overlaps outweigh its ~1 % per tile of bookkeeping.  Measured on
-  // GB300: +3.3 % at N = 8192 causal (1024 items of 33 tiles on average), -0.7 % at N = 16384
-  // causal (65 tiles), -3 % at N = 2048 (2.5 items per SM).
+  // Dense: the persistent form pays for causal d = 128 when items are many (at least four per
+  // SM) and short (at most 48 key tiles on average): then the ~2.5 tiles' worth of set-up,
+  // first loads and epilogue per item that it overlaps outweigh its ~1 % per tile of
+  // bookkeeping.  Measured on GB300 against the one-item form (with its split P store):
+  // +0.8 % at N = 8192 causal GQA (1024 items of 33 tiles on average), -0.7 % at N = 16384
+  // causal (65 tiles), -3 % at N = 2048 (2.5 items per SM); non-causal N = 4096: -1 % at
+  // d = 128, -3.5 % at d = 64; d = 64 N = 8192 causal: -1.5 %.
   const long long kt = (Nk + BN - 1) / BN;
   const long long avg_tiles = causal ? (kt + 1) / 2 : kt;
-  if (items >= 4LL * sms && avg_tiles <= 48)
-    return launch_d<D, kDense, true>(maps, out, lay, B, H, Hkv, Nq, Nk, causal, scale, items, sms, stream);
+  if constexpr (D == 128) {
+    if (causal && items >= 4LL * sms && avg_tiles <= 48)
+      return launch_d<D, kDense, true>(maps, out, lay, B, H, Hkv, Nq, Nk, causal, scale, items, sms, stream);
+  }
   // One item per CTA, heaviest first: the CTAs running at once take the same pairs of every
   // (batch, head) plane.  When all planes' K and V exceed half of L2, take the planes in
   // groups whose K and V fit there (whole GQA groups), so that K and V are read from DRAM

@@ -1,9 +1,10 @@
-"""The persistent form of the bf16 prefill (dense layout, many short items: at least four
-(query-tile pair, batch, head) items per SM and at most 48 key tiles per item on average),
-against the float64 oracle.  Barrier phases there run on across the items a CTA takes, so
-these shapes cover item boundaries with unequal chain lengths (causal), a ragged last pair
-(N not a multiple of 256: chain B short or absent), GQA, d = 64, and causal cross-attention
-with N_q > N_k, where whole items attend no key at all (no K or V tile is loaded for them)."""
+"""The persistent form of the bf16 prefill (dense layout, causal, d = 128, many short items:
+at least four (query-tile pair, batch, head) items per SM and at most 48 key tiles per item
+on average), against the float64 oracle.  Barrier phases there run on across the items a CTA
+takes, so these shapes cover item boundaries with unequal chain lengths, a ragged last pair
+(N not a multiple of 256: chain B short or absent), GQA, and causal cross-attention with
+N_q > N_k, where whole items attend no key at all (no K or V tile is loaded for them).  The
+same shapes non-causal and at d = 64 run the one-item form and are checked alike."""
 import math
 
 import numpy as np
@@ -17,10 +18,10 @@ from tests.parity import check_lse, check_o
 pytestmark = pytest.mark.gpu
 
 
-def _uses_persistent_form(B, H, Nq, Nk, causal, sms):
+def _uses_persistent_form(B, H, Nq, Nk, causal, d, sms):
     items = ((Nq + 255) // 256) * B * H
     kt = (Nk + 127) // 128
-    return items >= 4 * sms and ((kt + 1) // 2 if causal else kt) <= 48
+    return d == 128 and causal and items >= 4 * sms and ((kt + 1) // 2 if causal else kt) <= 48
 
 
 def _inputs(B, H, Hkv, Nq, Nk, d, seed):
@@ -44,7 +45,7 @@ def _check_planes(o, lse, q, k, v, causal, scale, planes, what):
 def test_persistent_self_attention(cuda, causal, d, N):
     B, H, Hkv = 8, 32, 8
     sms = torch.cuda.get_device_properties(cuda).multi_processor_count
-    assert _uses_persistent_form(B, H, N, N, causal, sms)
+    assert _uses_persistent_form(B, H, N, N, causal, d, sms) == (causal and d == 128)
     q, k, v = _inputs(B, H, Hkv, N, N, d, seed=N + d + causal)
     attn_device_error(clear=True)
     o, lse = attn_fwd(q.to(cuda), k.to(cuda), v.to(cuda), causal=causal, scale=1 / math.sqrt(d))
@@ -61,7 +62,7 @@ def test_persistent_cross_attention(cuda, B, Nq, Nk):
     and the items made only of such rows load no tile; N_q < N_k: every row sees extra keys."""
     H, Hkv, d = 32, 8, 128
     sms = torch.cuda.get_device_properties(cuda).multi_processor_count
-    assert _uses_persistent_form(B, H, Nq, Nk, True, sms)
+    assert _uses_persistent_form(B, H, Nq, Nk, True, d, sms)
     q, k, v = _inputs(B, H, Hkv, Nq, Nk, d, seed=Nq + 3 * Nk)
     attn_device_error(clear=True)
     o, lse = attn_fwd_cross(q.to(cuda), k.to(cuda), v.to(cuda), causal=True, scale=1 / math.sqrt(d))
